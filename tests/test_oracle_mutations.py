@@ -1,0 +1,133 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and show that the pins
+catch each one: a pin that no mistake can fail would pin nothing.
+
+Each mutation patches one oracle function for the duration of one test; the
+assertion is that at least one check in ``pins.ALL_CHECKS`` fails.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.decode
+import oracle.formats
+import oracle.layer
+from tests import pins
+
+
+def _any_check_fails():
+    for check in pins.ALL_CHECKS:
+        try:
+            check(oracle)
+        except AssertionError:
+            return check.__name__
+        except Exception:  # a crash under the mutation also counts as caught
+            return check.__name__
+    return None
+
+
+def _e4m3_wrong_bias(code):
+    s, e, m = (code >> 7) & 1, (code >> 3) & 0xF, code & 7
+    if e == 0xF and m == 7:
+        return math.nan
+    mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 8)
+    return -mag if s else mag
+
+
+def _e4m3_no_subnormal(code):
+    s, e, m = (code >> 7) & 1, (code >> 3) & 0xF, code & 7
+    if e == 0xF and m == 7:
+        return math.nan
+    mag = 0.0 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+    return -mag if s else mag
+
+
+def _e2m1_sign_bit2(code):
+    s, e, m = (code >> 2) & 1, (code >> 1) & 1, code & 1
+    mag = m * 0.5 if e == 0 else (1 + m / 2.0)
+    return -mag if s else mag
+
+
+def _nvfp4_high_nibble_first(q, bs):
+    q = np.asarray(q, dtype=np.uint8)
+    swapped = ((q & 0xF) << 4) | (q >> 4)
+    return ORIG_DECODE_NVFP4(swapped.astype(np.uint8), bs)
+
+
+def _nvfp4_block_of_8(q, bs):
+    q = np.asarray(q, dtype=np.uint8)
+    bs = np.asarray(bs, dtype=np.uint8)
+    n, half = q.shape
+    k = 2 * half
+    codes = np.empty((n, k), dtype=np.uint8)
+    codes[:, 0::2] = q & 0xF
+    codes[:, 1::2] = q >> 4
+    t4, t8 = oracle.e2m1_table(), oracle.e4m3_table()
+    idx = np.minimum(np.arange(k) // 8, bs.shape[1] - 1)
+    return t4[codes] * t8[bs][:, idx]
+
+
+def _linear_no_transpose(x, w_hat, alpha=1.0):
+    xf = oracle.layer._activations(x)
+    w = np.asarray(w_hat, dtype=np.float64)
+    if xf.shape[-1] == w.shape[0] and w.shape[0] == w.shape[1]:
+        return float(alpha) * (xf @ w)
+    return float(alpha) * (xf @ w[:, ::-1].T)
+
+
+def _linear_drop_alpha(x, w_hat, alpha=1.0):
+    return ORIG_LINEAR(x, w_hat, 1.0)
+
+
+def _linear_abs_weights(x, w_hat, alpha=1.0):
+    return ORIG_LINEAR(x, np.abs(w_hat), alpha)
+
+
+def _linear_drop_last_k(x, w_hat, alpha=1.0):
+    xf = oracle.layer._activations(x)
+    w = np.asarray(w_hat, dtype=np.float64)
+    return float(alpha) * (xf[..., :-1] @ w[:, :-1].T)
+
+
+ORIG_DECODE_NVFP4 = oracle.decode.decode_nvfp4
+ORIG_LINEAR = oracle.layer.linear
+
+MUTATIONS = {
+    "e4m3_bias_8": [(oracle.formats, "_e4m3_value", _e4m3_wrong_bias)],
+    "e4m3_flush_subnormals": [(oracle.formats, "_e4m3_value", _e4m3_no_subnormal)],
+    "e2m1_sign_in_bit2": [(oracle.formats, "_e2m1_value", _e2m1_sign_bit2)],
+    "nvfp4_high_nibble_first": [(oracle.layer, "decode_nvfp4", _nvfp4_high_nibble_first),
+                                (oracle, "nvfp4_materialize",
+                                 lambda q, bs: _nvfp4_high_nibble_first(q, bs))],
+    "nvfp4_block_of_8": [(oracle.layer, "decode_nvfp4", _nvfp4_block_of_8),
+                         (oracle, "nvfp4_materialize", _nvfp4_block_of_8)],
+    "weight_not_transposed": [(oracle.layer, "linear", _linear_no_transpose)],
+    "scale_not_folded": [(oracle.layer, "linear", _linear_drop_alpha)],
+    "abs_of_weights": [(oracle.layer, "linear", _linear_abs_weights)],
+    "dropped_last_term": [(oracle.layer, "linear", _linear_drop_last_k)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, monkeypatch):
+    for mod, attr, repl in MUTATIONS[name]:
+        monkeypatch.setattr(mod, attr, repl)
+    caught = _any_check_fails()
+    assert caught is not None, f"no pin catches the planted mistake {name!r}"
+
+
+def test_grouped_minus_one_not_zeroed_is_caught(monkeypatch):
+    orig = oracle.layer.fp8_grouped_matmul
+
+    def leaky(a, w, offs, ids, scales=None, rows=None):
+        ids = [0 if int(i) == -1 else int(i) for i in np.asarray(ids).reshape(-1)]
+        return orig(a, w, offs, ids, scales, rows)
+
+    monkeypatch.setattr(oracle, "fp8_grouped_matmul", leaky)
+    assert _any_check_fails() is not None
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _any_check_fails() is None
