@@ -1,0 +1,257 @@
+"""Python binding of libgq: weight-only FP8 / NVFP4 linear layers on GB300.
+
+    out = alpha * x @ dequant(W)^T      (bf16 activations, fp32 accumulation)
+
+This module only marshals arguments: it checks torch tensors (device, dtype,
+contiguity), takes their device pointers and the current CUDA stream, and
+calls the C ABI declared in ``include/gq.h``.  Every step of the computation
+runs in the library's CUDA kernels; there is no other code path.  If
+``libgq.so`` has not been built, or the current device is not an sm_103 GPU,
+the calls raise.
+
+Entry points (same names as the C ABI without the ``gq_`` prefix):
+``fp8_gemv``, ``nvfp4_gemv``, ``fp8_matmul``, ``nvfp4_matmul``,
+``fp8_grouped_matmul``, ``fp8_materialize``, ``nvfp4_materialize``.
+Host-buffer variants for end-to-end timing live in ``host``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgq.so")
+
+GQ_F32, GQ_BF16 = 0, 1
+
+# Names and argument types of every exported symbol (mirrors include/gq.h).
+_P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+SIGNATURES = {
+    "gq_status_str": (ctypes.c_char_p, [_I]),
+    "gq_version": (ctypes.c_char_p, []),
+    "gq_fp8_gemv": (_I, [_P, _I, _P, _P, _I64, _I64, _F, _P]),
+    "gq_nvfp4_gemv": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _F, _P]),
+    "gq_fp8_matmul": (_I, [_P, _I, _P, _P, _I64, _I64, _I64, _F, _P]),
+    "gq_nvfp4_matmul": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _F, _P]),
+    "gq_fp8_grouped_matmul": (_I, [_P, _I, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                   _I64, _I64, _P]),
+    "gq_fp8_materialize": (_I, [_P, _I, _P, _I64, _I64, _P]),
+    "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
+    "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
+}
+
+
+class GQError(RuntimeError):
+    """A libgq call returned a non-zero gq_status."""
+
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libgq.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"libgq.so not found at {p}: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load_library().gq_status_str(int(status)).decode()
+
+
+def version() -> str:
+    return load_library().gq_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise GQError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.float32:
+        return GQ_F32
+    if dtype == torch.bfloat16:
+        return GQ_BF16
+    raise TypeError("output dtype must be torch.float32 or torch.bfloat16")
+
+
+def _out(out, shape, dtype, device):
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must have shape {tuple(shape)}")
+    return out
+
+
+def _u8(t, name, ndim):
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    return t, _dev(t, name, torch.uint8, ndim)
+
+
+def fp8_gemv(x, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
+    """y[N] = alpha * x[K] @ e4m3(w[N, K])^T."""
+    w, wp = _u8(w, "w", 2)
+    n, k = w.shape
+    xp = _dev(x.reshape(-1), "x", torch.bfloat16, 1)
+    if x.numel() != k:
+        raise ValueError("x must have K elements")
+    dtype = out.dtype if out is not None else out_dtype
+    y = _out(out, (n,), dtype, w.device)
+    _check(load_library().gq_fp8_gemv(_dev(y, "out"), _out_code(dtype), xp, wp, n, k,
+                                      float(alpha), _stream_handle(stream)), "fp8_gemv")
+    return y
+
+
+def nvfp4_gemv(x, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
+    """y[N] = alpha * x[K] @ (e2m1(q) * e4m3(bs))^T;  q [N, K/2], bs [N, K/16]."""
+    q, qp = _u8(q, "q", 2)
+    bs, bp = _u8(bs, "bs", 2)
+    n, half = q.shape
+    k = 2 * half
+    xp = _dev(x.reshape(-1), "x", torch.bfloat16, 1)
+    if x.numel() != k or tuple(bs.shape) != (n, k // 16):
+        raise ValueError("shapes must be x [K], q [N, K/2], bs [N, K/16]")
+    dtype = out.dtype if out is not None else out_dtype
+    y = _out(out, (n,), dtype, q.device)
+    _check(load_library().gq_nvfp4_gemv(_dev(y, "out"), _out_code(dtype), xp, qp, bp, n, k,
+                                        float(alpha), _stream_handle(stream)), "nvfp4_gemv")
+    return y
+
+
+def fp8_matmul(a, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
+    """c[M, N] = alpha * a[M, K] @ e4m3(w[N, K])^T."""
+    w, wp = _u8(w, "w", 2)
+    ap = _dev(a, "a", torch.bfloat16, 2)
+    m, k = a.shape
+    n = w.shape[0]
+    if w.shape[1] != k:
+        raise ValueError("a and w disagree on K")
+    dtype = out.dtype if out is not None else out_dtype
+    c = _out(out, (m, n), dtype, a.device)
+    _check(load_library().gq_fp8_matmul(_dev(c, "out"), _out_code(dtype), ap, wp, m, n, k,
+                                        float(alpha), _stream_handle(stream)), "fp8_matmul")
+    return c
+
+
+def nvfp4_matmul(a, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
+    """c[M, N] = alpha * a[M, K] @ (e2m1(q) * e4m3(bs))^T."""
+    q, qp = _u8(q, "q", 2)
+    bs, bp = _u8(bs, "bs", 2)
+    ap = _dev(a, "a", torch.bfloat16, 2)
+    m, k = a.shape
+    n = q.shape[0]
+    if q.shape[1] * 2 != k or tuple(bs.shape) != (n, k // 16):
+        raise ValueError("shapes must be a [M, K], q [N, K/2], bs [N, K/16]")
+    dtype = out.dtype if out is not None else out_dtype
+    c = _out(out, (m, n), dtype, a.device)
+    _check(load_library().gq_nvfp4_matmul(_dev(c, "out"), _out_code(dtype), ap, qp, bp, m, n, k,
+                                          float(alpha), _stream_handle(stream)), "nvfp4_matmul")
+    return c
+
+
+def fp8_grouped_matmul(a, w, a_offsets, expert_ids, expert_scales=None, max_rows_per_group=None,
+                       out=None, out_dtype=torch.bfloat16, stream=None):
+    """Grouped MoE product.  a [total_M, K] bf16, w [E, N, K] e4m3,
+    a_offsets [G+1] uint32/int32 (device), expert_ids [G] int32 (device),
+    expert_scales [E] float32 or None.  Rows no group covers are left as they
+    are in `out` (allocate it yourself to control them)."""
+    w, wp = _u8(w, "w", 3)
+    ap = _dev(a, "a", torch.bfloat16, 2)
+    total_m, k = a.shape
+    e, n, kw = w.shape
+    if kw != k:
+        raise ValueError("a and w disagree on K")
+    if a_offsets.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("a_offsets must be int32 or uint32")
+    op = _dev(a_offsets, "a_offsets", None, 1)
+    ip = _dev(expert_ids, "expert_ids", torch.int32, 1)
+    g = expert_ids.numel()
+    if a_offsets.numel() != g + 1:
+        raise ValueError("a_offsets must have G + 1 entries")
+    sp = None if expert_scales is None else _dev(expert_scales, "expert_scales", torch.float32, 1)
+    if max_rows_per_group is None:
+        max_rows_per_group = total_m
+    dtype = out.dtype if out is not None else out_dtype
+    c = _out(out, (total_m, n), dtype, a.device)
+    _check(load_library().gq_fp8_grouped_matmul(
+        _dev(c, "out"), _out_code(dtype), ap, wp, op, ip, sp, g, e, int(max_rows_per_group),
+        total_m, n, k, _stream_handle(stream)), "fp8_grouped_matmul")
+    return c
+
+
+def fp8_materialize(w, out=None, out_dtype=torch.bfloat16, stream=None):
+    """Dense e4m3(w) [N, K] as float32 or bf16 (exact, unscaled)."""
+    w, wp = _u8(w, "w", 2)
+    n, k = w.shape
+    dtype = out.dtype if out is not None else out_dtype
+    o = _out(out, (n, k), dtype, w.device)
+    _check(load_library().gq_fp8_materialize(_dev(o, "out"), _out_code(dtype), wp, n, k,
+                                             _stream_handle(stream)), "fp8_materialize")
+    return o
+
+
+def nvfp4_materialize(q, bs, out=None, out_dtype=torch.bfloat16, stream=None):
+    """Dense e2m1(q) * e4m3(bs) [N, K] as float32 or bf16 (exact, unscaled)."""
+    q, qp = _u8(q, "q", 2)
+    bs, bp = _u8(bs, "bs", 2)
+    n, half = q.shape
+    k = 2 * half
+    dtype = out.dtype if out is not None else out_dtype
+    o = _out(out, (n, k), dtype, q.device)
+    _check(load_library().gq_nvfp4_materialize(_dev(o, "out"), _out_code(dtype), qp, bp, n, k,
+                                               _stream_handle(stream)), "nvfp4_materialize")
+    return o
+
+
+def device_status(reset: bool = False) -> int:
+    """Status flags recorded by bounded in-kernel waits that ran out (synchronizes)."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().gq_device_status(ctypes.byref(v), 1 if reset else 0), "device_status")
+    return int(v.value)
+
+
+__all__ = [
+    "fp8_gemv", "nvfp4_gemv", "fp8_matmul", "nvfp4_matmul", "fp8_grouped_matmul",
+    "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
+    "SIGNATURES", "LIB_PATH", "version", "status_str",
+]

@@ -1,0 +1,132 @@
+// common.cuh -- device helpers shared by the gq kernels (sm_103a).
+//
+// Number-format conversions use the hardware cvt instructions, which are
+// exact for every code of the narrow formats:
+//   float8_e4m3fn pair -> f16x2   (cvt.rn.f16x2.e4m3x2)
+//   E2M1 pair (one byte, low nibble = first element) -> f16x2
+//                                  (cvt.rn.f16x2.e2m1x2)
+// Every E4M3 and E2M1 value (and every E2M1 x E4M3 product) is exact in f16,
+// f32 and bf16, so the widenings below never round.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace gq {
+
+// Status bits recorded by bounded waits that ran out (see gq_device_status).
+enum : uint32_t {
+  kStatusTimeoutProducer = 1u << 0,
+  kStatusTimeoutMma = 1u << 1,
+  kStatusTimeoutDequant = 1u << 2,
+  kStatusTimeoutEpilogue = 1u << 3,
+  kStatusTimeoutOther = 1u << 4,
+};
+
+// ------------------------------------------------------------------ loads --
+
+// 16-byte streaming load: read once, do not keep in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// Cached read-only loads (activations are re-read by many CTAs).
+__device__ __forceinline__ uint4 ld_ro_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ld_ro_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_ro_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------------------ conversions --
+
+// Two float8_e4m3fn codes (low byte = first element) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t out;
+  const uint16_t in16 = static_cast<uint16_t>(two_codes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(in16));
+  return out;
+}
+
+// One byte of two E2M1 codes (low nibble = first element) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low8) {
+  uint32_t out;
+  const uint16_t in16 = static_cast<uint16_t>(byte_in_low8 & 0xFFu);
+  asm("{\n\t.reg .b8 lo, hi;\n\t"
+      "mov.b16 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "h"(in16));
+  return out;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = h2;
+  return __half22float2(h);
+}
+
+// bf16x2 bit patterns -> two floats (exact: bf16 is the top half of f32).
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// One float8_e4m3fn code -> float (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  return f16x2_to_f32x2(e4m3x2_to_f16x2(code & 0xFFu)).x;
+}
+
+// ----------------------------------------------------------------- stores --
+
+template <typename OutT> struct OutConv;
+template <> struct OutConv<float> {
+  static __device__ __forceinline__ float cvt(float v) { return v; }
+};
+template <> struct OutConv<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 cvt(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Pack two floats into bf16x2 bits with round-to-nearest-even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void record_status(uint32_t* status, uint32_t bit) {
+  if (status != nullptr) atomicOr(status, bit);
+}
+
+}  // namespace gq

@@ -1,0 +1,656 @@
+// gemm.cu -- W8A16 / W4A16 GEMMs and the grouped (MoE) W8A16 GEMM on the
+// 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+//   C[m, n] = alpha * sum_k A[m, k] * w_hat[n, k]      (A bf16, fp32 accumulate)
+//
+// Sources: the "fp4_matmul" kernel page (AppleM5Fp4MatMul: the packed weight
+// stays packed in memory, each (BN, BK) weight sub-tile is dequantized to bf16
+// once per K-strip into shared memory, cooperatively, and a dense bf16 MMA
+// reads it from there; the weight is the B operand, stored [N, K] row-major);
+// the "fp8_gemv" page (enqueue_apple_fp8_matmul: the raw W8A16 matmul with the
+// per-tensor scale folded after it); the "Matmul2dFp8" page (run_grouped: one
+// expert group per z, ragged rows from a_offsets, empty groups and out-of-range
+// M tiles skipped, expert id -1 writes zeros, per-expert scale after the sum).
+//
+// GB300 design (one persistent CTA per SM, warp-specialized):
+//   warp 0        TMA producer: A tile [128 x 64] bf16 (128-byte swizzle) and
+//                 the raw weight tile [256 x 64 codes] (FP8) or
+//                 [256 x 32 bytes] + block scales (NVFP4) into a ring of
+//                 kRawStages shared-memory stages, completion via mbarriers.
+//   warps 4..11   dequant: each thread owns one weight row of the tile, decodes
+//                 it exactly to bf16 and writes it in the 128-byte-swizzled
+//                 K-major layout the tensor core reads, into a ring of
+//                 kDeqStages stages.  Replaces the pages' barrier-fenced
+//                 cooperative decode; here it overlaps the MMA of other stages.
+//   warp 1        MMA issuer: one thread issues tcgen05.mma kind::f16
+//                 (M=128, N=256, K=16) x4 per 64-wide K step into a TMEM
+//                 accumulator (2 x 256 columns, double-buffered across tiles)
+//                 and releases stages with tcgen05.commit.
+//   warps 12..15  epilogue: tcgen05.ld the accumulator, multiply by the scale,
+//                 convert (RNE) and store with bounds guards.
+// Tiles are visited m-fastest so that consecutive CTAs share a weight tile
+// through L2 (the pages' Morton raster serves the same purpose).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int BM = 128;          // A rows per tile (MMA M)
+constexpr int BN = 256;          // weight rows per tile (MMA N)
+constexpr int BK = 64;           // K per stage (one 128-byte swizzle row of bf16)
+constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
+constexpr int kRawStages = 4;
+constexpr int kDeqStages = 2;
+constexpr int kThreads = 512;    // 16 warps
+constexpr int kWarpTma = 0;
+constexpr int kWarpMma = 1;
+constexpr int kDeqWarp0 = 4;
+constexpr int kDeqWarps = 8;     // 256 threads: one weight row each
+constexpr int kEpiWarp0 = 12;    // 4 warps: TMEM lane groups 0..3
+constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators
+
+constexpr uint32_t kABytes = BM * BK * 2;        // 16 KB
+constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
+
+enum class Fmt { kFp8, kNvfp4 };
+
+template <Fmt F> struct RawLayout;
+template <> struct RawLayout<Fmt::kFp8> {
+  static constexpr uint32_t kWBytes = BN * BK;          // 16 KB, 64-byte swizzle
+  static constexpr uint32_t kScaleBytes = 0;
+};
+template <> struct RawLayout<Fmt::kNvfp4> {
+  static constexpr uint32_t kWBytes = BN * BK / 2;      // 8 KB, 32-byte swizzle
+  static constexpr uint32_t kScaleBytes = BN * BK / 16; // 1 KB, 4 bytes per row
+};
+
+template <Fmt F> struct Smem {
+  static constexpr uint32_t kDeqOff = 0;
+  static constexpr uint32_t kAOff = kDeqOff + kDeqStages * kDeqBytes;
+  static constexpr uint32_t kWOff = kAOff + kRawStages * kABytes;
+  static constexpr uint32_t kSOff = kWOff + kRawStages * RawLayout<F>::kWBytes;
+  static constexpr uint32_t kBarOff = (kSOff + kRawStages * RawLayout<F>::kScaleBytes + 7) & ~7u;
+  // barriers: full_raw, empty_raw (kRawStages each), full_deq, empty_deq
+  // (kDeqStages each), tmem_full, tmem_empty (2 each), drain (1)
+  static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;   // tmem addr, abort flag
+  static constexpr uint32_t kTotal = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kTotal + 1024;              // slack for 1 KB alignment
+};
+
+// Work description shared by the plain and grouped GEMMs.
+struct Problem {
+  void* out;
+  const uint32_t* a_offsets;   // grouped only
+  const int32_t* expert_ids;   // grouped only
+  const float* expert_scales;  // grouped only (may be null)
+  uint32_t* status;
+  float alpha;
+  int M, N, K;                 // M = total rows for grouped
+  int num_n_tiles;
+  int num_k_blocks;
+  int G, E, max_rows;          // grouped only
+  int bf16_out;
+};
+
+// A tile of work: rows [m0, m_end) of C, columns [n0, n0 + BN), weight index.
+struct Tile {
+  int m0, m_end, n0, expert;  // expert: -1 = write zeros, >= 0 = weight matrix index
+  float scale;
+  bool valid;
+};
+
+// Plain GEMM: tile t -> (m tile fastest, n tile).
+__device__ __forceinline__ Tile plain_tile(const Problem& p, int t) {
+  const int num_m = (p.M + BM - 1) / BM;
+  Tile tl;
+  tl.m0 = (t % num_m) * BM;
+  tl.m_end = min(tl.m0 + BM, p.M);
+  tl.n0 = (t / num_m) * BN;
+  tl.expert = 0;
+  tl.scale = p.alpha;
+  tl.valid = true;
+  return tl;
+}
+
+__device__ __forceinline__ int plain_num_tiles(const Problem& p) {
+  return ((p.M + BM - 1) / BM) * p.num_n_tiles;
+}
+
+// Grouped GEMM: the work list is every (group, m tile, n tile) whose group has
+// rows, enumerated group by group, n tile, then m tile (fastest).  Each role
+// derives it from a_offsets / expert_ids (read-only device data) by a scan over
+// the groups, so no host synchronization and no scratch memory are needed.
+__device__ __forceinline__ int group_rows(const Problem& p, int z, int* start) {
+  int s = static_cast<int>(min(__ldg(p.a_offsets + z), static_cast<uint32_t>(p.M)));
+  int e = static_cast<int>(min(__ldg(p.a_offsets + z + 1), static_cast<uint32_t>(p.M)));
+  *start = s;
+  int rows = e > s ? e - s : 0;
+  return min(rows, p.max_rows);
+}
+
+__device__ __forceinline__ int grouped_num_tiles(const Problem& p) {
+  int total = 0;
+  for (int z = 0; z < p.G; ++z) {
+    int s;
+    const int rows = group_rows(p, z, &s);
+    total += ((rows + BM - 1) / BM) * p.num_n_tiles;
+  }
+  return total;
+}
+
+__device__ __forceinline__ Tile grouped_tile(const Problem& p, int t) {
+  Tile tl;
+  tl.valid = false;
+  for (int z = 0; z < p.G; ++z) {
+    int s;
+    const int rows = group_rows(p, z, &s);
+    const int mt = (rows + BM - 1) / BM;
+    const int cnt = mt * p.num_n_tiles;
+    if (t < cnt) {
+      tl.m0 = s + (t % mt) * BM;
+      tl.m_end = min(tl.m0 + BM, s + rows);
+      tl.n0 = (t / mt) * BN;
+      const int id = __ldg(p.expert_ids + z);
+      tl.expert = (id >= 0 && id < p.E) ? id : -1;
+      tl.scale = (tl.expert >= 0 && p.expert_scales != nullptr) ? __ldg(p.expert_scales + tl.expert)
+                                                                   : 1.0f;
+      tl.valid = true;
+      return tl;
+    }
+    t -= cnt;
+  }
+  return tl;
+}
+
+template <bool kGrouped>
+__device__ __forceinline__ Tile get_tile(const Problem& p, int t) {
+  if constexpr (kGrouped) return grouped_tile(p, t);
+  else return plain_tile(p, t);
+}
+
+template <bool kGrouped>
+__device__ __forceinline__ int num_tiles(const Problem& p) {
+  if constexpr (kGrouped) return grouped_num_tiles(p);
+  else return plain_num_tiles(p);
+}
+
+// ------------------------------------------------------------- dequant --
+
+// 16 FP8 codes -> 16 bf16 (two 16-byte chunks), exact, NaN preserved.
+__device__ __forceinline__ void fp8x16_to_bf16(uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(w[i] & 0xFFFFu));
+    const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2(w[i] >> 16));
+    o[2 * i] = pack_bf16x2(a.x, a.y);
+    o[2 * i + 1] = pack_bf16x2(b.x, b.y);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale ->
+// 16 bf16, exact (the product has at most 6 significant bits).
+__device__ __forceinline__ void nvfp4x16_to_bf16(uint32_t w0, uint32_t w1, float scale, uint4& lo,
+                                                 uint4& hi) {
+  const uint32_t w[2] = {w0, w1};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 e = f16x2_to_f32x2(e2m1x2_to_f16x2(w[i] >> (8 * j)));
+      o[4 * i + j] = pack_bf16x2(e.x * scale, e.y * scale);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Byte offset of the 16-byte chunk `j` of row `r` in a K-major tile stored
+// with the 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// ----------------------------------------------------------------- kernel --
+
+template <Fmt F, bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+          const uint8_t* __restrict__ scales_g, Problem p) {
+  using L = Smem<F>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full_raw = bars;
+  uint64_t* empty_raw = bars + kRawStages;
+  uint64_t* full_deq = bars + 2 * kRawStages;
+  uint64_t* empty_deq = full_deq + kDeqStages;
+  uint64_t* tmem_full = empty_deq + kDeqStages;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain = tmem_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t smem_base = tc::smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    constexpr uint32_t kRawArrivals = (F == Fmt::kNvfp4) ? 1 + 32 : 1;
+    for (int s = 0; s < kRawStages; ++s) {
+      tc::mbar_init(&full_raw[s], kRawArrivals);
+      tc::mbar_init(&empty_raw[s], 1 + kDeqWarps);
+    }
+    for (int s = 0; s < kDeqStages; ++s) {
+      tc::mbar_init(&full_deq[s], kDeqWarps);
+      tc::mbar_init(&empty_deq[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&tmem_full[s], 1);
+      tc::mbar_init(&tmem_empty[s], 4);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0 && p.num_k_blocks > 0 && (!kGrouped || p.E > 0)) {
+    tc::tma_prefetch_desc(&tmap_a);
+    tc::tma_prefetch_desc(&tmap_w);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_tiles = num_tiles<kGrouped>(p);
+  const int nkb = p.num_k_blocks;
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------ TMA producer --
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = get_tile<kGrouped>(p, t);
+      if (!tl.valid || tl.expert < 0) continue;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_dst = smem + L::kAOff + s * kABytes;
+        uint8_t* w_dst = smem + L::kWOff + s * RawLayout<F>::kWBytes;
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(&full_raw[s], kABytes + RawLayout<F>::kWBytes);
+          tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0);
+          if constexpr (F == Fmt::kFp8) {
+            if constexpr (kGrouped) {
+              tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * BK, tl.n0, tl.expert);
+            } else {
+              tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * BK, tl.n0);
+            }
+          } else {
+            tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * (BK / 2), tl.n0);
+          }
+        }
+        if constexpr (F == Fmt::kNvfp4) {
+          // Block scales: 4 bytes (4 blocks of 16) per weight row per stage.
+          uint8_t* s_dst = smem + L::kSOff + s * RawLayout<F>::kScaleBytes;
+          const int ks = p.K / 16;
+#pragma unroll
+          for (int i = 0; i < BN / 32; ++i) {
+            const int r = lane + 32 * i;
+            const int n = tl.n0 + r;
+            const bool in = n < p.N;
+            const uint8_t* src = scales_g + (static_cast<int64_t>(in ? n : 0) * ks + kb * 4);
+            tc::cp_async_4(s_dst + r * 4, src, in ? 4u : 0u);
+          }
+          tc::cp_async_mbar_arrive_noinc(&full_raw[s]);
+        }
+        if (++s == kRawStages) { s = 0; ph ^= 1; }
+      }
+    }
+    // Drain: make sure no copy issued by this warp is still landing in shared
+    // memory when the CTA exits (bounded; normally already complete).
+    if (lane == 0) {
+      int ds = s;
+      uint32_t dph = ph;
+      for (int i = 0; i < kRawStages; ++i) {
+        if (--ds < 0) { ds = kRawStages - 1; dph ^= 1; }
+        tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------- MMA issuer --
+    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(BM, BN);
+    int s = 0, d = 0;
+    uint32_t ph = 0, dph = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = get_tile<kGrouped>(p, t);
+      if (!tl.valid || tl.expert < 0) continue;
+      const int acc = it & 1;
+      const uint32_t acc_ph = (it >> 1) & 1;
+      ++it;
+      if (!tc::mbar_wait(&tmem_empty[acc], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
+      tc::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma) ||
+            !tc::mbar_wait(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_base + L::kAOff + s * kABytes;
+          const uint32_t b_addr = smem_base + L::kDeqOff + d * kDeqBytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
+            const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
+            tc::mma_bf16(d_tmem, ad, bd, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&empty_raw[s]);
+          tc::mma_commit(&empty_deq[d]);
+        }
+        __syncwarp();
+        if (++s == kRawStages) { s = 0; ph ^= 1; }
+        if (++d == kDeqStages) { d = 0; dph ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc::mma_commit(&tmem_full[acc]);
+      __syncwarp();
+    }
+    // Drain: every MMA issued by this thread completes before TMEM is freed.
+    if (lane == 0) {
+      tc::mma_commit(drain);
+      tc::mbar_wait_quiet(drain, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+    // ---------------------------------------------------------- dequant --
+    const int row = threadIdx.x - kDeqWarp0 * 32;  // 0..255: weight row in the tile
+    int s = 0, d = 0;
+    uint32_t ph = 0, dph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = get_tile<kGrouped>(p, t);
+      if (!tl.valid || tl.expert < 0) continue;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant) ||
+            !tc::mbar_wait(&empty_deq[d], dph ^ 1, abort_flag, p.status, kStatusTimeoutDequant)) {
+          ok = false;
+          break;
+        }
+        const uint32_t w_addr = smem_base + L::kWOff + s * RawLayout<F>::kWBytes;
+        const uint32_t b_addr = smem_base + L::kDeqOff + d * kDeqBytes;
+        if constexpr (F == Fmt::kFp8) {
+          // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = tc::lds128(w_addr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+            uint4 lo, hi;
+            fp8x16_to_bf16(v, lo, hi);
+            tc::sts128(b_addr + sw128_off(row, 2 * c), lo);
+            tc::sts128(b_addr + sw128_off(row, 2 * c + 1), hi);
+          }
+        } else {
+          // Row of 32 packed bytes, TMA 32-byte swizzle: chunk c at c ^ ((row >> 2) & 1).
+          const uint32_t sc = tc::lds32(smem_base + L::kSOff + s * RawLayout<F>::kScaleBytes + row * 4);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 v = tc::lds128(w_addr + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
+            const float s0 = e4m3_to_f32(sc >> (16 * c));
+            const float s1 = e4m3_to_f32(sc >> (16 * c + 8));
+            uint4 lo, hi;
+            nvfp4x16_to_bf16(v.x, v.y, s0, lo, hi);
+            tc::sts128(b_addr + sw128_off(row, 4 * c), lo);
+            tc::sts128(b_addr + sw128_off(row, 4 * c + 1), hi);
+            nvfp4x16_to_bf16(v.z, v.w, s1, lo, hi);
+            tc::sts128(b_addr + sw128_off(row, 4 * c + 2), lo);
+            tc::sts128(b_addr + sw128_off(row, 4 * c + 3), hi);
+          }
+        }
+        tc::fence_proxy_async_smem();   // make the generic stores visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(&full_deq[d]);
+          tc::mbar_arrive(&empty_raw[s]);
+        }
+        if (++s == kRawStages) { s = 0; ph ^= 1; }
+        if (++d == kDeqStages) { d = 0; dph ^= 1; }
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // --------------------------------------------------------- epilogue --
+    const int g = warp & 3;                 // TMEM lane group of this warp
+    const int r_local = g * 32 + lane;      // accumulator row (tile-local)
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const Tile tl = get_tile<kGrouped>(p, t);
+      if (!tl.valid) continue;
+      const int m = tl.m0 + r_local;
+      const bool row_ok = m < tl.m_end;
+      if (tl.expert < 0) {
+        // Inactive group: write zeros for its rows, no tensor-core work.
+        if (row_ok) {
+          for (int c = 0; c < BN && tl.n0 + c < p.N; ++c) {
+            const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0 + c;
+            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+            else static_cast<float*>(p.out)[o] = 0.f;
+          }
+        }
+        continue;
+      }
+      const int acc = it & 1;
+      const uint32_t acc_ph = (it >> 1) & 1;
+      ++it;
+      if (!tc::mbar_wait(&tmem_full[acc], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + acc * BN;
+      const bool vec_ok = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(taddr + c0, r);
+        tc::tmem_wait_ld();
+        const int n = tl.n0 + c0;
+        if (!row_ok || n >= p.N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+        const int64_t o = static_cast<int64_t>(m) * p.N + n;
+        if (vec_ok && n + 32 <= p.N) {
+          if (p.bf16_out) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        } else {
+          const int lim = min(32, p.N - n);
+          for (int i = 0; i < lim; ++i) {
+            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + i] = __float2bfloat16_rn(v[i]);
+            else static_cast<float*>(p.out)[o + i] = v[i];
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[acc]);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Writes alpha * 0 (K = 0: the sum is empty).
+__global__ void k_fill_scaled_zero(void* out, int bf16_out, int64_t count, float alpha) {
+  const float v = alpha * 0.f;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (bf16_out) static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+    else static_cast<float*>(out)[i] = v;
+  }
+}
+
+// --------------------------------------------------------------- host --
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0, d0 * d1};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <Fmt F, bool kGrouped>
+cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, const uint8_t* scales,
+                   const Problem& p, int grid) {
+  auto kern = k_wq_gemm<F, kGrouped>;
+  const uint32_t smem = Smem<F>::kAlloc;
+  // The shared-memory opt-in is set once per device (it is not a stream
+  // operation, so it is kept out of any CUDA-graph capture after the first call).
+  static std::atomic<uint64_t> configured{0};
+  const uint64_t bit = 1ull << (c.device & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kern<<<grid, kThreads, smem, c.stream>>>(ta, tw, scales, p);
+  return cudaGetLastError();
+}
+
+cudaError_t fill_zero(const Ctx& c, void* out, bool bf16_out, int64_t count, float alpha) {
+  const int grid = static_cast<int>(std::min<int64_t>((count + 255) / 256, c.num_sms * 8LL));
+  k_fill_scaled_zero<<<grid > 0 ? grid : 1, 256, 0, c.stream>>>(out, bf16_out ? 1 : 0, count, alpha);
+  return cudaGetLastError();
+}
+
+Problem base_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_t N, int64_t K,
+                     float alpha) {
+  Problem p{};
+  p.out = out;
+  p.status = c.status;
+  p.alpha = alpha;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
+  p.bf16_out = bf16_out ? 1 : 0;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* a, const uint8_t* w,
+                            int64_t M, int64_t N, int64_t K, float alpha) {
+  if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
+  CUtensorMap ta, tw;
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
+  const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
+  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, std::min(tiles, c.num_sms));
+}
+
+cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+                              const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N, int64_t K,
+                              float alpha) {
+  if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
+  CUtensorMap ta, tw;
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K / 2, N, K / 2, BK / 2, BN,
+                 CU_TENSOR_MAP_SWIZZLE_32B))
+    return cudaErrorInvalidValue;
+  Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
+  const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
+  return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, std::min(tiles, c.num_sms));
+}
+
+cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+                                    const uint8_t* w, const uint32_t* a_offsets,
+                                    const int32_t* expert_ids, const float* expert_scales,
+                                    int64_t G, int64_t E, int64_t max_rows, int64_t total_M,
+                                    int64_t N, int64_t K) {
+  // With no weights or an empty sum every covered row is zero: the kernel's
+  // zero path handles that when no expert is valid (E = 0), and no tensor map
+  // is touched.
+  CUtensorMap ta, tw;
+  memset(&ta, 0, sizeof(ta));
+  memset(&tw, 0, sizeof(tw));
+  if (E > 0 && K > 0) {
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, total_M, K * 2, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&tw, w, K, N, E, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
+  Problem p = base_problem(c, out, bf16_out, total_M, N, K, 1.0f);
+  p.a_offsets = a_offsets;
+  p.expert_ids = expert_ids;
+  p.expert_scales = expert_scales;
+  p.G = static_cast<int>(G);
+  p.E = (K > 0) ? static_cast<int>(E) : 0;
+  p.max_rows = static_cast<int>(std::min<int64_t>(max_rows, total_M));
+  // Upper bound of the work list (the exact count needs the device offsets).
+  const int64_t mt = (p.max_rows + BM - 1) / BM;
+  const int64_t bound = std::min<int64_t>(G * mt * p.num_n_tiles, 1LL << 30);
+  const int grid = static_cast<int>(std::min<int64_t>(bound, c.num_sms));
+  return launch<Fmt::kFp8, true>(c, ta, tw, nullptr, p, grid > 0 ? grid : 1);
+}
+
+}  // namespace gq

@@ -1,0 +1,328 @@
+// gemv.cu -- M = 1 decode GEMVs for FP8 and NVFP4 weights.
+//
+//   y[n] = alpha * sum_k x[k] * w_hat[n, k]
+//
+// Source: the "fp8_gemv" kernel page (fp8_gemv_kernel: the batch-1 decode
+// product is a matrix-vector product with no MMA to feed; lanes stride down K
+// in vector-wide chunks, widen the FP8 weight to f32 in registers, fp32 FMA,
+// warp sum, narrow tail) and, for NVFP4, the same page's description of the
+// FP4 sibling (nibble unpack, E2M1 decode, per-16 FP8 block scale) with the
+// layout of the "fp4_matmul" page.
+//
+// GB300 design.  The kernel is HBM-bound: every weight byte is read exactly
+// once and nothing else is large.  A CTA of 8 warps owns R consecutive rows
+// and splits K across all 256 threads (thread t takes vectors t, t+256, ...),
+// so each thread streams R rows x U vectors of 16-byte weight loads before it
+// does any arithmetic (deep memory-level parallelism: ~32 KB in flight per
+// CTA), and the bf16 activation chunk it loads once is reused for all R rows.
+// The R partial sums are reduced with xor-shuffles inside each warp and then
+// across the 8 warps in a fixed order through shared memory (deterministic).
+// Weight loads bypass L1 (read once); activation loads go through L1 because
+// every CTA on the SM reads the same x.
+//
+// The load width adapts to K and the pointers: 16 bytes when K % 16 == 0,
+// down to 1 byte for odd K (the pages' scalar tail for K % TILE_K != 0 becomes
+// a narrower vector for the whole row, so no row ever straddles an unaligned
+// vector).
+#include "common.cuh"
+#include "internal.h"
+
+namespace gq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// ---------------------------------------------------------------- helpers --
+
+// Load VEC bf16 activations starting at element k0 and widen to f32.
+template <int VEC>
+__device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t k0, float* xf) {
+  if constexpr (VEC == 16) {
+    const uint4 a = ld_ro_v4(x + k0);
+    const uint4 b = ld_ro_v4(x + k0 + 8);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      xf[2 * i] = bf16lo_to_f32(v[i]);
+      xf[2 * i + 1] = bf16hi_to_f32(v[i]);
+    }
+  } else if constexpr (VEC == 8) {
+    const uint4 a = ld_ro_v4(x + k0);
+    const uint32_t v[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xf[2 * i] = bf16lo_to_f32(v[i]);
+      xf[2 * i + 1] = bf16hi_to_f32(v[i]);
+    }
+  } else if constexpr (VEC == 4) {
+    const uint2 a = ld_ro_v2(x + k0);
+    xf[0] = bf16lo_to_f32(a.x);
+    xf[1] = bf16hi_to_f32(a.x);
+    xf[2] = bf16lo_to_f32(a.y);
+    xf[3] = bf16hi_to_f32(a.y);
+  } else if constexpr (VEC == 2) {
+    const uint32_t a = ld_ro_u32(x + k0);
+    xf[0] = bf16lo_to_f32(a);
+    xf[1] = bf16hi_to_f32(a);
+  } else {
+    xf[0] = __uint_as_float(static_cast<uint32_t>(x[k0]) << 16);
+  }
+}
+
+// Load VEC fp8 codes (VEC bytes) of one row as 32-bit words (VEC < 4: one
+// word holding the codes in its low bytes).
+template <int VEC>
+__device__ __forceinline__ void load_w8(const uint8_t* __restrict__ p, uint32_t* words) {
+  if constexpr (VEC == 16) {
+    const uint4 a = ld_stream_v4(p);
+    words[0] = a.x; words[1] = a.y; words[2] = a.z; words[3] = a.w;
+  } else if constexpr (VEC == 8) {
+    const uint2 a = ld_stream_v2(p);
+    words[0] = a.x; words[1] = a.y;
+  } else if constexpr (VEC == 4) {
+    words[0] = ld_stream_u32(p);
+  } else if constexpr (VEC == 2) {
+    words[0] = *reinterpret_cast<const uint16_t*>(p);
+  } else {
+    words[0] = *p;
+  }
+}
+
+// acc += sum over the VEC codes of x * e4m3(code).
+template <int VEC>
+__device__ __forceinline__ float fma_fp8(const uint32_t* words, const float* xf, float acc) {
+  constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) {
+    if constexpr (VEC >= 2) {
+      const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(words[i] & 0xFFFFu));
+      acc = fmaf(xf[4 * i + 0], lo.x, acc);
+      acc = fmaf(xf[4 * i + 1], lo.y, acc);
+      if constexpr (VEC >= 4) {
+        const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(words[i] >> 16));
+        acc = fmaf(xf[4 * i + 2], hi.x, acc);
+        acc = fmaf(xf[4 * i + 3], hi.y, acc);
+      }
+    } else {
+      acc = fmaf(xf[0], e4m3_to_f32(words[0]), acc);
+    }
+  }
+  return acc;
+}
+
+template <int R>
+__device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, int64_t row0,
+                                                 int64_t N, float alpha, void* y, bool bf16_out) {
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xFFFFFFFFu, acc[r], off);
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) red[warp * R + r] = acc[r];
+  }
+  __syncthreads();
+  if (threadIdx.x < R) {
+    const int r = threadIdx.x;
+    float s = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < kWarps; ++wi) s += red[wi * R + r];
+    const int64_t n = row0 + r;
+    if (n < N) {
+      const float v = alpha * s;
+      if (bf16_out) {
+        static_cast<__nv_bfloat16*>(y)[n] = __float2bfloat16_rn(v);
+      } else {
+        static_cast<float*>(y)[n] = v;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------- FP8 --
+
+template <int VEC, int R, int U>
+__global__ void __launch_bounds__(kThreads)
+k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
+           const uint8_t* __restrict__ w, int64_t N, int64_t K, float alpha) {
+  __shared__ float red[kWarps * R];
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int64_t nvec = K / VEC;
+  constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+
+  // Rows past N (last CTA) re-read the last valid row and are never stored.
+  const uint8_t* rows[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t n = row0 + r < N ? row0 + r : N - 1;
+    rows[r] = w + n * K;
+  }
+
+  int64_t v = threadIdx.x;
+  // Main loop: U vectors per step, all loads issued before the math.
+  for (; v + static_cast<int64_t>(U - 1) * kThreads < nvec; v += static_cast<int64_t>(U) * kThreads) {
+    uint32_t wv[U][R][kWords];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + (v + u * kThreads) * VEC, wv[u][r]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float xf[VEC];
+      load_x<VEC>(x, (v + u * kThreads) * VEC, xf);
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[u][r], xf, acc[r]);
+    }
+  }
+  // Remainder: fewer than U vectors left for this thread.
+  for (; v < nvec; v += kThreads) {
+    uint32_t wv[R][kWords];
+#pragma unroll
+    for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + v * VEC, wv[r]);
+    float xf[VEC];
+    load_x<VEC>(x, v * VEC, xf);
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[r], xf, acc[r]);
+  }
+  reduce_and_store<R>(acc, red, row0, N, alpha, y, bf16_out);
+}
+
+// ----------------------------------------------------------------- NVFP4 --
+
+// One vector = VB bytes of packed nibbles = 2*VB elements = VB/8 blocks.
+template <int VB>
+__device__ __forceinline__ float fma_nvfp4(const uint32_t* words, uint32_t scales,
+                                           const uint16_t* __restrict__ x, int64_t k0, float acc) {
+  constexpr int kBlocks = VB / 8;
+#pragma unroll
+  for (int b = 0; b < kBlocks; ++b) {
+    float xf[16];
+    load_x<16>(x, k0 + 16 * b, xf);
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t wd = words[2 * b + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 e = f16x2_to_f32x2(e2m1x2_to_f16x2(wd >> (8 * j)));
+        part = fmaf(xf[8 * i + 2 * j], e.x, part);
+        part = fmaf(xf[8 * i + 2 * j + 1], e.y, part);
+      }
+    }
+    acc = fmaf(part, e4m3_to_f32(scales >> (8 * b)), acc);
+  }
+  return acc;
+}
+
+template <int VB, int R, int U>
+__global__ void __launch_bounds__(kThreads)
+k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
+             const uint8_t* __restrict__ q, const uint8_t* __restrict__ bs, int64_t N,
+             int64_t K, float alpha) {
+  __shared__ float red[kWarps * R];
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
+  const int64_t half_k = K / 2;
+  const int64_t nvec = half_k / VB;
+  constexpr int kWords = VB / 4;
+  constexpr int kBlocks = VB / 8;
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  const uint8_t* qrows[R];
+  const uint8_t* srows[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t n = row0 + r < N ? row0 + r : N - 1;
+    qrows[r] = q + n * half_k;
+    srows[r] = bs + n * (K / 16);
+  }
+  auto load_scales = [&](const uint8_t* s, int64_t vv) -> uint32_t {
+    if constexpr (kBlocks == 2) {
+      return *reinterpret_cast<const uint16_t*>(s + vv * 2);
+    } else {
+      return s[vv];
+    }
+  };
+
+  int64_t v = threadIdx.x;
+  for (; v + static_cast<int64_t>(U - 1) * kThreads < nvec; v += static_cast<int64_t>(U) * kThreads) {
+    uint32_t wv[U][R][kWords];
+    uint32_t sv[U][R];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        load_w8<VB>(qrows[r] + (v + u * kThreads) * VB, wv[u][r]);
+        sv[u][r] = load_scales(srows[r], v + u * kThreads);
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        acc[r] = fma_nvfp4<VB>(wv[u][r], sv[u][r], x, (v + u * kThreads) * 2 * VB, acc[r]);
+  }
+  for (; v < nvec; v += kThreads) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      uint32_t wv[kWords];
+      load_w8<VB>(qrows[r] + v * VB, wv);
+      const uint32_t sv = load_scales(srows[r], v);
+      acc[r] = fma_nvfp4<VB>(wv, sv, x, v * 2 * VB, acc[r]);
+    }
+  }
+  reduce_and_store<R>(acc, red, row0, N, alpha, y, bf16_out);
+}
+
+constexpr int kRows = 4;
+
+template <int VEC>
+cudaError_t fp8_dispatch(const Ctx& c, void* y, bool bf16_out, const void* x,
+                         const uint8_t* w, int64_t N, int64_t K, float alpha) {
+  const int64_t grid = (N + kRows - 1) / kRows;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  k_fp8_gemv<VEC, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
+      y, bf16_out, static_cast<const uint16_t*>(x), w, N, K, alpha);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+                            const uint8_t* w, int64_t N, int64_t K, float alpha) {
+  const uintptr_t wa = reinterpret_cast<uintptr_t>(w);
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+  auto fits = [&](int vec) {
+    return K % vec == 0 && wa % vec == 0 && xa % (vec >= 8 ? 16 : 2 * vec) == 0;
+  };
+  if (fits(16)) return fp8_dispatch<16>(c, y, bf16_out, x, w, N, K, alpha);
+  if (fits(8)) return fp8_dispatch<8>(c, y, bf16_out, x, w, N, K, alpha);
+  if (fits(4)) return fp8_dispatch<4>(c, y, bf16_out, x, w, N, K, alpha);
+  if (fits(2)) return fp8_dispatch<2>(c, y, bf16_out, x, w, N, K, alpha);
+  return fp8_dispatch<1>(c, y, bf16_out, x, w, N, K, alpha);
+}
+
+cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+                              const uint8_t* q, const uint8_t* bs, int64_t N,
+                              int64_t K, float alpha) {
+  const int64_t grid = (N + kRows - 1) / kRows;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const bool wide = (K % 32 == 0) && (reinterpret_cast<uintptr_t>(bs) % 2 == 0);
+  if (wide) {
+    k_nvfp4_gemv<16, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
+        y, bf16_out, xb, q, bs, N, K, alpha);
+  } else {
+    k_nvfp4_gemv<8, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
+        y, bf16_out, xb, q, bs, N, K, alpha);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gq

@@ -1,0 +1,51 @@
+// internal.h -- host-side declarations shared between the gq translation units.
+// Not part of the public C ABI (that is include/gq.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gq {
+
+// Per-call launch context filled by the C-ABI layer.
+struct Ctx {
+  cudaStream_t stream;
+  uint32_t* status;   // device address of the per-device status word
+  int num_sms;        // multiprocessor count of the current device
+  int device;
+};
+
+// materialize.cu
+cudaError_t launch_fp8_materialize(const Ctx& c, void* out, bool bf16_out,
+                                   const uint8_t* w, int64_t total);
+cudaError_t launch_nvfp4_materialize(const Ctx& c, void* out, bool bf16_out,
+                                     const uint8_t* q, const uint8_t* bs,
+                                     int64_t total_blocks);
+
+// gemv.cu
+cudaError_t launch_fp8_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+                            const uint8_t* w, int64_t N, int64_t K, float alpha);
+cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+                              const uint8_t* q, const uint8_t* bs, int64_t N,
+                              int64_t K, float alpha);
+
+// gemm.cu
+cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+                            const uint8_t* w, int64_t M, int64_t N, int64_t K,
+                            float alpha);
+cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+                              const uint8_t* q, const uint8_t* bs, int64_t M,
+                              int64_t N, int64_t K, float alpha);
+cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out,
+                                    const void* a, const uint8_t* w,
+                                    const uint32_t* a_offsets,
+                                    const int32_t* expert_ids,
+                                    const float* expert_scales, int64_t G,
+                                    int64_t E, int64_t max_rows,
+                                    int64_t total_M, int64_t N, int64_t K);
+
+// api.cu: the driver's cuTensorMapEncodeTiled, resolved once at run time so
+// that the library does not link against libcuda.
+void* tensor_map_encode_fn();
+
+}  // namespace gq

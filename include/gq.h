@@ -1,0 +1,182 @@
+/*
+ * gq.h -- weight-only quantized linear layer for NVIDIA GB300 (sm_103a).
+ *
+ *     out = alpha * x @ dequant(W)^T          (bf16 activations, fp32 accumulation)
+ *
+ * Two weight formats:
+ *   FP8   -- float8_e4m3fn codes W[N, K], one byte per element, row-major; one
+ *            per-tensor scale (weight_scale) passed as `alpha`.
+ *            Source: the "fp8_gemv" kernel page (Modular API docs,
+ *            kernels/linalg/matmul/gpu/apple/fp8_gemv), first paragraph and
+ *            paragraph "Scale contract".
+ *   NVFP4 -- packed E2M1 nibbles q[N, K/2] (byte j of a row holds element 2j in
+ *            its low nibble and element 2j+1 in its high nibble) plus
+ *            float8_e4m3fn block scales bs[N, K/16], one per 16 consecutive
+ *            elements of a row; the per-tensor second scale (weight_scale_2)
+ *            is passed as `alpha`.  Source: the "fp4_matmul" kernel page
+ *            (kernels/linalg/matmul/gpu/apple/fp4_matmul), first paragraph.
+ *
+ * Common conventions for every entry point below
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller, dense row-major, and must stay valid until the work
+ *     queued on `stream` has finished.  The library allocates nothing and
+ *     keeps no pointer after the call returns.
+ *   - Work is queued on `stream` (0 = the legacy default stream); the call does
+ *     not synchronize.  Argument checks run on the host before anything is
+ *     queued; a non-zero status means nothing was queued.
+ *   - Activations are bfloat16 bit patterns.  Outputs are float32 or bfloat16
+ *     (`out_dtype`), converted from the fp32 result with round-to-nearest-even.
+ *   - `alpha` multiplies the fp32 sum once, before the output conversion
+ *     (alpha = 1 gives the raw product).  Because a scalar factors out of the
+ *     sum this equals folding the scale after the matmul.
+ *   - Pointer alignment: 16 bytes for every tensor pointer (weights,
+ *     activations, outputs); block scales need 1 byte.  Odd K is allowed for
+ *     the FP8 GEMV (it picks a narrower load width); see each call.
+ *   - Zero-sized M or N: nothing is queued, GQ_OK.  K = 0: outputs are written
+ *     as alpha * 0.
+ *   - Results are deterministic: a given call on given inputs returns the same
+ *     bits every time (fixed summation order, no atomics).
+ *   - Every wait inside the kernels is bounded; a wait that runs out records a
+ *     code in a per-device status word (gq_device_status) and the kernel
+ *     returns instead of hanging.
+ */
+#ifndef GQ_H_
+#define GQ_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQ_OK = 0,
+  GQ_ERR_NULL = 1,      /* a required pointer is NULL                         */
+  GQ_ERR_SHAPE = 2,     /* a size is negative or violates a format rule       */
+  GQ_ERR_ALIGN = 3,     /* a pointer is not aligned as required               */
+  GQ_ERR_DTYPE = 4,     /* unknown output dtype                               */
+  GQ_ERR_DEVICE = 5,    /* current device is not sm_103 or cannot be queried  */
+  GQ_ERR_LAUNCH = 6,    /* the kernel launch failed (cudaGetLastError)        */
+  GQ_ERR_TOO_LARGE = 7  /* a size exceeds what the kernel supports            */
+} gq_status;
+
+typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
+
+/* Human-readable name of a gq_status value (static string). */
+const char* gq_status_str(int status);
+
+/* Library version, e.g. "gq 0.1.0 sm_103a". */
+const char* gq_version(void);
+
+/*
+ * FP8 GEMV (M = 1 decode).  y[n] = alpha * sum_k x[k] * e4m3(w[n, k]).
+ * Source: "fp8_gemv" page -- enqueue_apple_fp8_gemv and fp8_gemv_kernel (one
+ * warp per output, lanes striding K, fp32 FMA, warp sum, narrow tail).
+ *   y      [N]    float32 or bfloat16 (out_dtype)
+ *   x      [K]    bfloat16
+ *   w      [N, K] float8_e4m3fn codes
+ * Any K >= 0.  Pointer alignment: 16 bytes gives the widest loads; less is
+ * accepted (the load width drops to what K and the pointers allow).
+ */
+int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w,
+                int64_t N, int64_t K, float alpha, cudaStream_t stream);
+
+/*
+ * NVFP4 GEMV (M = 1).  y[n] = alpha * sum_k x[k] * e2m1(q[n, k]) * e4m3(bs[n, k/16]).
+ * Source: "fp4_matmul" page (weight layout); the "fp8_gemv" page names this
+ * kernel as the FP4 sibling of its GEMV (nibble unpack, E2M1 decode, per-16
+ * FP8 block scale).
+ *   y [N] (out_dtype), x [K] bfloat16, q [N, K/2] uint8, bs [N, K/16] uint8.
+ * K % 16 == 0 (GQ_ERR_SHAPE otherwise).  q, x, y 16-byte aligned.
+ */
+int gq_nvfp4_gemv(void* y, int out_dtype, const void* x, const uint8_t* q,
+                  const uint8_t* bs, int64_t N, int64_t K, float alpha,
+                  cudaStream_t stream);
+
+/*
+ * FP8 GEMM (M >= 1).  c[m, n] = alpha * sum_k a[m, k] * e4m3(w[n, k]).
+ * Source: "fp8_gemv" page -- enqueue_apple_fp8_matmul (raw W8A16 matmul);
+ * "Matmul2dFp8" page (bf16 A x fp8 B -> fp32, c_type output).
+ *   c [M, N] (out_dtype), a [M, K] bfloat16, w [N, K] float8_e4m3fn.
+ * K % 16 == 0 (GQ_ERR_SHAPE otherwise): the tensor-memory-accelerator row
+ * stride rule.  M, N arbitrary.  Pointers 16-byte aligned.
+ */
+int gq_fp8_matmul(void* c, int out_dtype, const void* a, const uint8_t* w,
+                  int64_t M, int64_t N, int64_t K, float alpha,
+                  cudaStream_t stream);
+
+/*
+ * NVFP4 GEMM (M >= 1).  c = alpha * a @ dequant(q, bs)^T.
+ * Source: "fp4_matmul" page -- enqueue_apple_fp4_matmul and AppleM5Fp4MatMul
+ * (packed weight stays packed in memory; each weight tile is dequantized to
+ * bf16 once into shared memory and fed to a dense bf16 MMA).
+ *   c [M, N] (out_dtype), a [M, K] bf16, q [N, K/2] uint8, bs [N, K/16] uint8.
+ * K % 64 == 0 (GQ_ERR_SHAPE otherwise).  Pointers 16-byte aligned, bs 4-byte.
+ */
+int gq_nvfp4_matmul(void* c, int out_dtype, const void* a, const uint8_t* q,
+                    const uint8_t* bs, int64_t M, int64_t N, int64_t K,
+                    float alpha, cudaStream_t stream);
+
+/*
+ * Grouped (MoE) FP8 GEMM.  For every group z in [0, G):
+ *   rows r in [a_offsets[z], a_offsets[z+1]):
+ *     c[r, :] = 0                                     if expert_ids[z] == -1
+ *     c[r, :] = s_e * a[r, :] @ e4m3(w[e, :, :])^T    with e = expert_ids[z],
+ *               s_e = expert_scales[e] (1 when expert_scales is NULL)
+ * Source: "Matmul2dFp8" page, method run_grouped (ragged groups from
+ * a_offsets, empty groups do nothing, expert id -1 writes zeros, the
+ * per-expert scale folded after the product).
+ *   c             [total_M, N] (out_dtype)
+ *   a             [total_M, K] bfloat16
+ *   w             [E, N, K]    float8_e4m3fn, one weight per expert
+ *   a_offsets     [G + 1]      uint32, device memory
+ *   expert_ids    [G]          int32, device memory
+ *   expert_scales [E]          float32, device memory, or NULL (raw)
+ *   max_rows_per_group         an upper bound on a_offsets[z+1] - a_offsets[z]
+ * Device-side data is not checked on the host (that would need a sync); the
+ * kernel treats it defensively: an id outside [0, E) other than -1 is
+ * treated as -1, a group with a_offsets[z+1] <= a_offsets[z] is empty, rows
+ * outside [0, total_M) are never read or written, rows that no group covers
+ * are left untouched, and rows beyond max_rows_per_group in a group are not
+ * computed (out of contract).  K % 16 == 0.
+ */
+int gq_fp8_grouped_matmul(void* c, int out_dtype, const void* a,
+                          const uint8_t* w, const uint32_t* a_offsets,
+                          const int32_t* expert_ids, const float* expert_scales,
+                          int64_t G, int64_t E, int64_t max_rows_per_group,
+                          int64_t total_M, int64_t N, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * FP8 materialize: out[n, k] = e4m3(w[n, k]) as float32 or bfloat16, exact
+ * (every E4M3 value is representable in both), no scale applied.
+ * Source: "fp8_gemv" page -- enqueue_fp8_materialize / fp8_materialize_kernel.
+ *   out [N, K] (out_dtype), w [N, K].
+ */
+int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w,
+                       int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * NVFP4 materialize: out[n, k] = e2m1(q[n, k]) * e4m3(bs[n, k/16]), exact in
+ * float32 and bfloat16 (the product has at most 6 significant bits), no
+ * per-tensor scale applied.  Source: "fp4_matmul" page (weight layout); the
+ * NVFP4 counterpart of the FP8 materialize.
+ *   out [N, K] (out_dtype), q [N, K/2], bs [N, K/16].  K % 16 == 0.
+ */
+int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q,
+                         const uint8_t* bs, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/*
+ * Status word of the current device: bit flags recorded by kernels whose
+ * bounded waits ran out (0 = none).  Synchronizes the device.  If `reset` is
+ * non-zero the word is cleared afterwards.  Returns GQ_OK or GQ_ERR_DEVICE.
+ */
+int gq_device_status(uint32_t* flags, int reset);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* GQ_H_ */

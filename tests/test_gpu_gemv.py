@@ -1,0 +1,159 @@
+"""GEMV kernels (M = 1 decode) against the oracle.
+
+Tolerance (floating point): |gpu - oracle| <= 2e-4 * |alpha| * sum_k |x_k w_k|,
+plus one bf16 ulp of the result for bf16 outputs (``oracle.tolerance``).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_fp8_nvfp4_gb300 as gq
+import oracle
+import synth
+from tests.gpu_util import (DEV, assert_canary, assert_within, bits, canary_out, lib,
+                            to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fp8(n, k, out_dtype, alpha_mode="scale", seed=0, x_offset=0, w_offset=0):
+    codes, scale = synth.fp8_weight(n, k, seed=seed)
+    x = synth.bf16_activations(1, k, seed=seed + 1).reshape(-1)
+    alpha = scale if alpha_mode == "scale" else 1.0
+    # optional misalignment: place the tensors at an element offset
+    xs = torch.zeros(k + x_offset, dtype=torch.bfloat16, device=DEV)
+    xs[x_offset:] = x.to(DEV)
+    ws = torch.zeros(n * k + w_offset, dtype=torch.uint8, device=DEV)
+    ws[w_offset:] = codes.reshape(-1).to(DEV)
+    buf, y = canary_out((n,), out_dtype)
+    gq.fp8_gemv(xs[x_offset:], ws[w_offset:].view(n, k), alpha, out=y)
+    torch.cuda.synchronize()
+    got = to_f64(y)
+    w_hat = oracle.decode_fp8(codes.numpy())
+    xb = bits(x)
+    ref = oracle.fp8_gemv(xb, codes.numpy(), alpha)
+    tol = oracle.tolerance(xb[None, :], w_hat, alpha, out_dtype == torch.bfloat16,
+                           ref=ref[None, :])[0]
+    assert_within(got, ref, tol, f"fp8 gemv {n}x{k}")
+    assert_canary(buf)
+    return got
+
+
+# configs: N=256 K=512 / 520 fp32 (raw and scaled); decode shapes bf16 scaled
+@pytest.mark.parametrize("k", [512, 520])
+@pytest.mark.parametrize("alpha_mode", ["raw", "scale"])
+def test_fp8_gemv_small_config(k, alpha_mode):
+    lib()
+    run_fp8(256, k, torch.float32, alpha_mode)
+
+
+@pytest.mark.parametrize("n,k", [(4096, 4096), (14336, 4096), (4096, 14336)])
+def test_fp8_gemv_decode_shapes(n, k):
+    lib()
+    run_fp8(n, k, torch.bfloat16)
+
+
+@pytest.mark.parametrize("n", [1, 3, 127, 257])
+@pytest.mark.parametrize("k", [0, 1, 16, 17, 32, 520, 4112])
+def test_fp8_gemv_odd_shapes(n, k):
+    lib()
+    run_fp8(n, k, torch.float32, seed=n * 31 + k)
+
+
+@pytest.mark.parametrize("x_offset,w_offset", [(1, 0), (0, 3), (2, 8), (4, 4)])
+def test_fp8_gemv_misaligned_pointers(x_offset, w_offset):
+    lib()
+    run_fp8(65, 1024, torch.float32, x_offset=x_offset, w_offset=w_offset)
+
+
+def test_fp8_gemv_scale_fold_is_exact_and_deterministic():
+    """gemv(alpha) == fp32(gemv(1) * alpha) bit for bit, and repeat calls agree."""
+    lib()
+    codes, scale = synth.fp8_weight(1000, 4096, seed=5)
+    x = synth.bf16_activations(1, 4096, seed=6).reshape(-1).to(DEV)
+    w = codes.to(DEV)
+    raw = gq.fp8_gemv(x, w, 1.0, out_dtype=torch.float32)
+    scaled = gq.fp8_gemv(x, w, scale, out_dtype=torch.float32)
+    again = gq.fp8_gemv(x, w, scale, out_dtype=torch.float32)
+    assert torch.equal(scaled, again)
+    assert torch.equal(scaled, raw * torch.tensor(scale, dtype=torch.float32, device=DEV))
+
+
+def test_fp8_gemv_nan_code_propagates():
+    lib()
+    codes, _ = synth.fp8_weight(8, 256, seed=9)
+    codes[3, 100] = 0x7F
+    codes[5, 7] = 0xFF
+    x = synth.bf16_activations(1, 256, seed=10).reshape(-1)
+    got = gq.fp8_gemv(x.to(DEV), codes.to(DEV), 1.0, out_dtype=torch.float32).cpu().numpy()
+    ref = oracle.layer.linear_loops(bits(x), oracle.decode_fp8(codes.numpy()), 1.0)[0]
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.isnan(got[3]) and np.isnan(got[5])
+
+
+def test_fp8_gemv_equals_gemm_row_of_oracle():
+    """The GEMV of row i equals row i of the oracle's GEMM (within tolerance)."""
+    lib()
+    codes, scale = synth.fp8_weight(300, 2048, seed=12)
+    a = synth.bf16_activations(3, 2048, seed=13)
+    ref = oracle.fp8_matmul(bits(a), codes.numpy(), scale)
+    w_hat = oracle.decode_fp8(codes.numpy())
+    for i in range(3):
+        got = to_f64(gq.fp8_gemv(a[i].to(DEV), codes.to(DEV), scale, out_dtype=torch.float32))
+        tol = oracle.tolerance(bits(a)[i:i + 1], w_hat, scale)[0]
+        assert_within(got, ref[i], tol, f"row {i}")
+
+
+def run_nvfp4(n, k, out_dtype, seed=0):
+    q, bs, s2 = synth.nvfp4_weight(n, k, seed=seed)
+    x = synth.bf16_activations(1, k, seed=seed + 1).reshape(-1)
+    buf, y = canary_out((n,), out_dtype)
+    gq.nvfp4_gemv(x.to(DEV), q.to(DEV), bs.to(DEV), s2, out=y)
+    torch.cuda.synchronize()
+    got = to_f64(y)
+    xb = bits(x)
+    ref = oracle.nvfp4_gemv(xb, q.numpy(), bs.numpy(), s2)
+    w_hat = oracle.decode_nvfp4(q.numpy(), bs.numpy())
+    tol = oracle.tolerance(xb[None, :], w_hat, s2, out_dtype == torch.bfloat16, ref=ref[None, :])[0]
+    assert_within(got, ref, tol, f"nvfp4 gemv {n}x{k}")
+    assert_canary(buf)
+
+
+def test_nvfp4_gemv_config():
+    lib()
+    run_nvfp4(4096, 4096, torch.bfloat16)
+
+
+@pytest.mark.parametrize("n", [1, 3, 127, 257])
+@pytest.mark.parametrize("k", [0, 16, 32, 48, 4112])
+def test_nvfp4_gemv_odd_shapes(n, k):
+    lib()
+    run_nvfp4(n, k, torch.float32, seed=n + 7 * k)
+
+
+def test_nvfp4_gemv_worked_example():
+    """The hand-worked example of tests/golden/nvfp4_gemv_worked.txt."""
+    lib()
+    from tests import pins
+    rows = pins._rows("nvfp4_gemv_worked.txt")
+    q = torch.tensor([[int(c, 16) for c in rows["q"][0]]], dtype=torch.uint8, device=DEV)
+    bs = torch.tensor([[int(c, 16) for c in rows["bs"][0]]], dtype=torch.uint8, device=DEV)
+    x = torch.tensor([float(v) for v in rows["x"][0]], dtype=torch.bfloat16, device=DEV)
+    y = gq.nvfp4_gemv(x, q, bs, float(rows["alpha"][0][0]), out_dtype=torch.float32)
+    assert y.item() == float(rows["scaled"][0][0])
+
+
+def test_gemv_errors():
+    l = lib()
+    s = torch.cuda.current_stream().cuda_stream
+    w = torch.zeros(4, 32, dtype=torch.uint8, device=DEV)
+    x = torch.zeros(32, dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros(4, dtype=torch.float32, device=DEV)
+    assert l.gq_fp8_gemv(y.data_ptr(), 0, None, w.data_ptr(), 4, 32, 1.0, s) == 1
+    assert l.gq_fp8_gemv(y.data_ptr(), 0, x.data_ptr(), w.data_ptr(), 4, -2, 1.0, s) == 2
+    assert l.gq_fp8_gemv(y.data_ptr(), 5, x.data_ptr(), w.data_ptr(), 4, 32, 1.0, s) == 4
+    assert l.gq_nvfp4_gemv(y.data_ptr(), 0, x.data_ptr(), w.data_ptr(), w.data_ptr(), 4, 24,
+                           1.0, s) == 2
+    assert l.gq_nvfp4_gemv(y.data_ptr(), 0, x.data_ptr() + 2, w.data_ptr(), w.data_ptr(), 4, 32,
+                           1.0, s) == 3
+    assert l.gq_fp8_gemv(y.data_ptr(), 0, x.data_ptr(), w.data_ptr(), 0, 32, 1.0, s) == 0
