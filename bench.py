@@ -2,7 +2,8 @@
 """Benchmark of the weight-only quantized linear layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--headline-only] [--no-cpu-baseline] [--only nvfp4|gemm|grouped]
+                    [--headline-only] [--no-cpu-baseline]
+                    [--only nvfp4|gemm|grouped|gemv-shapes]
 
 Prints ONE JSON line (rank 0).  The headline `value` is the M=1 FP8 (W8A16)
 decode GEMV throughput in GB/s of algorithmic bytes over one step = the three
@@ -302,7 +303,7 @@ def run_ours(args, rank, local, world):
             "unit": "GB/s",
             "frac": round(value / world / peaks["hbm_gbs"], 4),
             "peak_source": peaks["source"],
-            "kernel": "k_fp8_gemv<16,4,2>",
+            "kernel": "k_fp8_gemv<16,4,4,128>",
             "traffic": committed_traffic("fp8_gemv"),
             "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         },
@@ -577,7 +578,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the FP8 GEMV headline (no sub-benchmarks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["nvfp4", "gemm", "grouped"], default=None,
+    ap.add_argument("--only", choices=["nvfp4", "gemm", "grouped", "gemv-shapes"], default=None,
                     help="run one sub-benchmark alone and print its result (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -592,12 +593,38 @@ def main():
     run_ours(args, rank, local, world)
 
 
+def gemv_shape_times(gq, dev, stream, steps, warm):
+    """Per-launch time of each FP8 decode shape alone (rotating weight copies)."""
+    import synth
+    out = {}
+    for n, k in GEMV_SHAPES:
+        codes, s = synth.fp8_weight(n, k, seed=0)
+        x = synth.bf16_activations(1, k, seed=1).reshape(-1).to(dev)
+        copies = n_copies(n * k)
+        ws = [codes.to(dev) for _ in range(copies)]
+        y = torch.empty(n, dtype=torch.bfloat16, device=dev)
+
+        def step(i, ws=ws, x=x, y=y, s=s):
+            gq.fp8_gemv(x, ws[i % copies], s, out=y, stream=stream)
+
+        ms = graph_timer(step, steps, warm, min(steps, 200), stream, 1)
+        t = ms * 1e-3 / steps
+        out[f"{n}x{k}"] = {"us": round(t * 1e6, 3), "GB/s": round(fp8_gemv_bytes(n, k) / t / 1e9, 1)}
+        del ws
+    return out
+
+
 def run_only(args, local):
     import gemm_fp8_nvfp4_gb300 as gq
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     gq.load_library()
     stream = torch.cuda.Stream(device=dev)
+    if args.only == "gemv-shapes":
+        print(json.dumps({"only": args.only,
+                          "shapes": gemv_shape_times(gq, dev, stream, args.steps, args.warmup)}),
+              flush=True)
+        return
     subs = run_subs(args, gq, dev, stream, measured_peaks(), 1, only=args.only)
     print(json.dumps({"only": args.only, "sub": subs}), flush=True)
 

@@ -30,8 +30,7 @@
 namespace gq {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 128;   // threads per CTA (8 CTAs fit on an SM)
 
 // ---------------------------------------------------------------- helpers --
 
@@ -89,6 +88,71 @@ __device__ __forceinline__ void load_w8(const uint8_t* __restrict__ p, uint32_t*
   }
 }
 
+// Two e4m3 codes in each half of a 32-bit word -> two f16x2 (hardware cvt,
+// exact); the half selection is part of the instruction.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// f16x2 -> (f32, f32).
+__device__ __forceinline__ float2 h2f2(uint32_t h) {
+  float a, b;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(h));
+  return make_float2(a, b);
+}
+
+// acc += a * b on both halves: one packed fp32 FMA (fma.rn.f32x2).
+__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<unsigned long long*>(&acc)));
+  acc = *reinterpret_cast<float2*>(&r);
+}
+
+// bf16x2 bit patterns -> (f32, f32), exact.
+__device__ __forceinline__ float2 bf2f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// Byte B (0..3) of a word holds two E2M1 codes -> f16x2 (hardware cvt, exact).
+template <int B>
+__device__ __forceinline__ uint32_t e2m1x2_b(uint32_t w) {
+  uint32_t out;
+  if constexpr (B == 0) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(out) : "r"(w));
+  } else if constexpr (B == 1) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+        : "=r"(out) : "r"(w));
+  } else if constexpr (B == 2) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+        : "=r"(out) : "r"(w));
+  } else {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+        : "=r"(out) : "r"(w));
+  }
+  return out;
+}
+
+// 16 fp8 codes (4 words) x 16 activations (8 f32 pairs) into a pair
+// accumulator: 8 cvt, 8 x 2 cvt.f32.f16 and 8 packed FMAs.
+__device__ __forceinline__ void dot16_fp8(const uint32_t* w, const float2* xf, float2& acc) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h01, h23;
+    e4m3x4_to_h2x2(w[q], h01, h23);
+    ffma2(acc, h2f2(h01), xf[2 * q]);
+    ffma2(acc, h2f2(h23), xf[2 * q + 1]);
+  }
+}
+
 // acc += sum over the VEC codes of x * e4m3(code).
 template <int VEC>
 __device__ __forceinline__ float fma_fp8(const uint32_t* words, const float* xf, float acc) {
@@ -111,7 +175,7 @@ __device__ __forceinline__ float fma_fp8(const uint32_t* words, const float* xf,
   return acc;
 }
 
-template <int R>
+template <int R, int T>
 __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, int64_t row0,
                                                  int64_t N, float alpha, void* y, bool bf16_out) {
 #pragma unroll
@@ -130,7 +194,7 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
     const int r = threadIdx.x;
     float s = 0.f;
 #pragma unroll
-    for (int wi = 0; wi < kWarps; ++wi) s += red[wi * R + r];
+    for (int wi = 0; wi < T / 32; ++wi) s += red[wi * R + r];
     const int64_t n = row0 + r;
     if (n < N) {
       const float v = alpha * s;
@@ -145,17 +209,15 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
 
 // ------------------------------------------------------------------- FP8 --
 
-template <int VEC, int R, int U>
-__global__ void __launch_bounds__(kThreads)
+template <int VEC, int R, int U, int T = kThreads>
+__global__ void __launch_bounds__(T)
 k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
            const uint8_t* __restrict__ w, int64_t N, int64_t K, float alpha) {
-  __shared__ float red[kWarps * R];
+  constexpr int kThreads = T;
+  __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t nvec = K / VEC;
   constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
-  float acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
 
   // Rows past N (last CTA) re-read the last valid row and are never stored.
   const uint8_t* rows[R];
@@ -165,76 +227,131 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
     rows[r] = w + n * K;
   }
 
-  int64_t v = threadIdx.x;
-  // Main loop: U vectors per step, all loads issued before the math.
-  for (; v + static_cast<int64_t>(U - 1) * kThreads < nvec; v += static_cast<int64_t>(U) * kThreads) {
-    uint32_t wv[U][R][kWords];
+  float acc[R];
+  if constexpr (VEC == 16) {
+    // 16 codes per vector; the activations are widened once per vector and
+    // reused for the R rows; pair accumulators fed by packed FMAs.
+    float2 acc2[R];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int r = 0; r < R; ++r) acc2[r] = make_float2(0.f, 0.f);
+    int64_t v = threadIdx.x;
+    for (; v + static_cast<int64_t>(U - 1) * kThreads < nvec; v += static_cast<int64_t>(U) * kThreads) {
+      uint4 wv[U][R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + (v + u * kThreads) * VEC, wv[u][r]);
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+        for (int r = 0; r < R; ++r) wv[u][r] = ld_stream_v4(rows[r] + (v + u * kThreads) * 16);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint4 xa = ld_ro_v4(x + (v + u * kThreads) * 16);
+        const uint4 xb = ld_ro_v4(x + (v + u * kThreads) * 16 + 8);
+        const float2 xf[8] = {bf2f2(xa.x), bf2f2(xa.y), bf2f2(xa.z), bf2f2(xa.w),
+                              bf2f2(xb.x), bf2f2(xb.y), bf2f2(xb.z), bf2f2(xb.w)};
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint32_t ww[4] = {wv[u][r].x, wv[u][r].y, wv[u][r].z, wv[u][r].w};
+          dot16_fp8(ww, xf, acc2[r]);
+        }
+      }
+    }
+    for (; v < nvec; v += kThreads) {
+      uint4 wv[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) wv[r] = ld_stream_v4(rows[r] + v * 16);
+      const uint4 xa = ld_ro_v4(x + v * 16);
+      const uint4 xb = ld_ro_v4(x + v * 16 + 8);
+      const float2 xf[8] = {bf2f2(xa.x), bf2f2(xa.y), bf2f2(xa.z), bf2f2(xa.w),
+                            bf2f2(xb.x), bf2f2(xb.y), bf2f2(xb.z), bf2f2(xb.w)};
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+        dot16_fp8(ww, xf, acc2[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = acc2[r].x + acc2[r].y;
+  } else {
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+    int64_t v = threadIdx.x;
+    for (; v + static_cast<int64_t>(U - 1) * kThreads < nvec; v += static_cast<int64_t>(U) * kThreads) {
+      uint32_t wv[U][R][kWords];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + (v + u * kThreads) * VEC, wv[u][r]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float xf[VEC];
+        load_x<VEC>(x, (v + u * kThreads) * VEC, xf);
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[u][r], xf, acc[r]);
+      }
+    }
+    for (; v < nvec; v += kThreads) {
+      uint32_t wv[R][kWords];
+#pragma unroll
+      for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + v * VEC, wv[r]);
       float xf[VEC];
-      load_x<VEC>(x, (v + u * kThreads) * VEC, xf);
+      load_x<VEC>(x, v * VEC, xf);
 #pragma unroll
-      for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[u][r], xf, acc[r]);
+      for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[r], xf, acc[r]);
     }
   }
-  // Remainder: fewer than U vectors left for this thread.
-  for (; v < nvec; v += kThreads) {
-    uint32_t wv[R][kWords];
-#pragma unroll
-    for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + v * VEC, wv[r]);
-    float xf[VEC];
-    load_x<VEC>(x, v * VEC, xf);
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[r], xf, acc[r]);
-  }
-  reduce_and_store<R>(acc, red, row0, N, alpha, y, bf16_out);
+  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
 }
 
 // ----------------------------------------------------------------- NVFP4 --
 
-// One vector = VB bytes of packed nibbles = 2*VB elements = VB/8 blocks.
+// One vector = VB bytes of packed nibbles = 2*VB elements = VB/8 blocks; xf
+// holds the vector's activations as f32 pairs (VB pairs).
 template <int VB>
-__device__ __forceinline__ float fma_nvfp4(const uint32_t* words, uint32_t scales,
-                                           const uint16_t* __restrict__ x, int64_t k0, float acc) {
+__device__ __forceinline__ void dot_nvfp4(const uint32_t* words, uint32_t scales, const float2* xf,
+                                          float2& acc) {
   constexpr int kBlocks = VB / 8;
 #pragma unroll
   for (int b = 0; b < kBlocks; ++b) {
-    float xf[16];
-    load_x<16>(x, k0 + 16 * b, xf);
-    float part = 0.f;
+    float2 part = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t wd = words[2 * b + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 e = f16x2_to_f32x2(e2m1x2_to_f16x2(wd >> (8 * j)));
-        part = fmaf(xf[8 * i + 2 * j], e.x, part);
-        part = fmaf(xf[8 * i + 2 * j + 1], e.y, part);
-      }
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t wd = words[2 * b + q];
+      ffma2(part, h2f2(e2m1x2_b<0>(wd)), xf[8 * b + 4 * q + 0]);
+      ffma2(part, h2f2(e2m1x2_b<1>(wd)), xf[8 * b + 4 * q + 1]);
+      ffma2(part, h2f2(e2m1x2_b<2>(wd)), xf[8 * b + 4 * q + 2]);
+      ffma2(part, h2f2(e2m1x2_b<3>(wd)), xf[8 * b + 4 * q + 3]);
     }
-    acc = fmaf(part, e4m3_to_f32(scales >> (8 * b)), acc);
+    const float s = e4m3_to_f32(scales >> (8 * b));
+    ffma2(acc, part, make_float2(s, s));
   }
-  return acc;
 }
 
-template <int VB, int R, int U>
-__global__ void __launch_bounds__(kThreads)
+template <int VB>
+__device__ __forceinline__ void load_xf(const uint16_t* __restrict__ x, int64_t k0, float2* xf) {
+#pragma unroll
+  for (int q = 0; q < VB / 4; ++q) {
+    const uint4 xv = ld_ro_v4(x + k0 + 8 * q);
+    xf[4 * q + 0] = bf2f2(xv.x);
+    xf[4 * q + 1] = bf2f2(xv.y);
+    xf[4 * q + 2] = bf2f2(xv.z);
+    xf[4 * q + 3] = bf2f2(xv.w);
+  }
+}
+
+template <int VB, int R, int U, int T = kThreads>
+__global__ void __launch_bounds__(T)
 k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
              const uint8_t* __restrict__ q, const uint8_t* __restrict__ bs, int64_t N,
              int64_t K, float alpha) {
-  __shared__ float red[kWarps * R];
+  constexpr int kThreads = T;
+  __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t half_k = K / 2;
   const int64_t nvec = half_k / VB;
   constexpr int kWords = VB / 4;
   constexpr int kBlocks = VB / 8;
-  float acc[R];
+  float2 acc2[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int r = 0; r < R; ++r) acc2[r] = make_float2(0.f, 0.f);
   const uint8_t* qrows[R];
   const uint8_t* srows[R];
 #pragma unroll
@@ -263,21 +380,30 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
         sv[u][r] = load_scales(srows[r], v + u * kThreads);
       }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
+      float2 xf[VB];
+      load_xf<VB>(x, (v + u * kThreads) * 2 * VB, xf);
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-        acc[r] = fma_nvfp4<VB>(wv[u][r], sv[u][r], x, (v + u * kThreads) * 2 * VB, acc[r]);
-  }
-  for (; v < nvec; v += kThreads) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      uint32_t wv[kWords];
-      load_w8<VB>(qrows[r] + v * VB, wv);
-      const uint32_t sv = load_scales(srows[r], v);
-      acc[r] = fma_nvfp4<VB>(wv, sv, x, v * 2 * VB, acc[r]);
+      for (int r = 0; r < R; ++r) dot_nvfp4<VB>(wv[u][r], sv[u][r], xf, acc2[r]);
     }
   }
-  reduce_and_store<R>(acc, red, row0, N, alpha, y, bf16_out);
+  for (; v < nvec; v += kThreads) {
+    uint32_t wv[R][kWords];
+    uint32_t sv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      load_w8<VB>(qrows[r] + v * VB, wv[r]);
+      sv[r] = load_scales(srows[r], v);
+    }
+    float2 xf[VB];
+    load_xf<VB>(x, v * 2 * VB, xf);
+#pragma unroll
+    for (int r = 0; r < R; ++r) dot_nvfp4<VB>(wv[r], sv[r], xf, acc2[r]);
+  }
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = acc2[r].x + acc2[r].y;
+  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
 }
 
 constexpr int kRows = 4;
@@ -287,7 +413,7 @@ cudaError_t fp8_dispatch(const Ctx& c, void* y, bool bf16_out, const void* x,
                          const uint8_t* w, int64_t N, int64_t K, float alpha) {
   const int64_t grid = (N + kRows - 1) / kRows;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  k_fp8_gemv<VEC, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
+  k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
       y, bf16_out, static_cast<const uint16_t*>(x), w, N, K, alpha);
   return cudaGetLastError();
 }

@@ -157,3 +157,14 @@ def test_gemv_errors():
     assert l.gq_nvfp4_gemv(y.data_ptr(), 0, x.data_ptr() + 2, w.data_ptr(), w.data_ptr(), 4, 32,
                            1.0, s) == 3
     assert l.gq_fp8_gemv(y.data_ptr(), 0, x.data_ptr(), w.data_ptr(), 0, 32, 1.0, s) == 0
+
+
+@pytest.mark.parametrize("n,k", [(1, 4096), (151, 4096), (152, 256), (153, 768), (5000, 2048),
+                                 (7, 16384), (2, 32768)])
+def test_gemv_row_splits(n, k):
+    """Row counts below, at and above the SM count, ragged last CTA, long rows
+    (the multi-vector unrolled loop plus its remainder) and short ones."""
+    lib()
+    run_fp8(n, k, torch.float32, seed=n)
+    if k % 32 == 0:
+        run_nvfp4(n, k, torch.float32, seed=n + 1)
