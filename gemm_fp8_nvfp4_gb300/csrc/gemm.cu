@@ -13,7 +13,7 @@
 // M tiles skipped, expert id -1 writes zeros, per-expert scale after the sum).
 //
 // GB300 design (one persistent CTA per SM, warp-specialized):
-//   warp 0        TMA producer: A tile [128 x 64] bf16 (128-byte swizzle) and
+//   warp 0        TMA producer: A tile [256 x 64] bf16 (128-byte swizzle) and
 //                 the raw weight tile [256 x 64 codes] (FP8) or
 //                 [256 x 32 bytes] + block scales (NVFP4) into a ring of
 //                 kRawStages shared-memory stages, completion via mbarriers.
@@ -23,11 +23,15 @@
 //                 kDeqStages stages.  Replaces the pages' barrier-fenced
 //                 cooperative decode; here it overlaps the MMA of other stages.
 //   warp 1        MMA issuer: one thread issues tcgen05.mma kind::f16
-//                 (M=128, N=256, K=16) x4 per 64-wide K step into a TMEM
-//                 accumulator (2 x 256 columns, double-buffered across tiles)
-//                 and releases stages with tcgen05.commit.
-//   warps 12..15  epilogue: tcgen05.ld the accumulator, multiply by the scale,
-//                 convert (RNE) and store with bounds guards.
+//                 (M=128, N=256, K=16): per 16-wide K slice two MMAs, one per
+//                 128-row half of the A tile, both reading the same dequantized
+//                 weight tile -- so each decoded weight and each byte of
+//                 weight traffic through shared memory serves 256 rows of A
+//                 (shared-memory bandwidth bounds this kernel).  The two
+//                 256-column fp32 accumulators fill TMEM; stages are released
+//                 with tcgen05.commit.
+//   warps 12..15  epilogue: tcgen05.ld both accumulators, multiply by the
+//                 scale, convert (RNE) and store with bounds guards.
 // Tiles are visited m-fastest so that consecutive CTAs share a weight tile
 // through L2 (the pages' Morton raster serves the same purpose).
 #include <cuda.h>
@@ -44,11 +48,12 @@
 namespace gq {
 namespace {
 
-constexpr int BM = 128;          // A rows per tile (MMA M)
+constexpr int BM = 256;          // A rows per tile (two MMA halves)
+constexpr int UMMA_M = 128;      // rows per tcgen05.mma
 constexpr int BN = 256;          // weight rows per tile (MMA N)
 constexpr int BK = 64;           // K per stage (one 128-byte swizzle row of bf16)
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
-constexpr int kRawStages = 4;
+constexpr int kRawStages = 3;
 constexpr int kDeqStages = 2;
 constexpr int kThreads = 512;    // 16 warps
 constexpr int kWarpTma = 0;
@@ -56,9 +61,10 @@ constexpr int kWarpMma = 1;
 constexpr int kDeqWarp0 = 4;
 constexpr int kDeqWarps = 8;     // 256 threads: one weight row each
 constexpr int kEpiWarp0 = 12;    // 4 warps: TMEM lane groups 0..3
-constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators
+constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators (one per A half)
 
-constexpr uint32_t kABytes = BM * BK * 2;        // 16 KB
+constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
+constexpr uint32_t kAHalfBytes = UMMA_M * BK * 2;  // 16 KB: offset of the second A half
 constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
 
 enum class Fmt { kFp8, kNvfp4 };
@@ -192,8 +198,10 @@ __device__ __forceinline__ void fp8x16_to_bf16(uint4 v, uint4& lo, uint4& hi) {
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(w[i] & 0xFFFFu));
-    const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2(w[i] >> 16));
+    uint32_t h01, h23;
+    e4m3x4_to_h2x2(w[i], h01, h23);
+    const float2 a = h2f2(h01);
+    const float2 b = h2f2(h23);
     o[2 * i] = pack_bf16x2(a.x, a.y);
     o[2 * i + 1] = pack_bf16x2(b.x, b.y);
   }
@@ -341,7 +349,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
-    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(BM, BN);
+    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(UMMA_M, BN);
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     int it = 0;
@@ -349,12 +357,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
-      const int acc = it & 1;
-      const uint32_t acc_ph = (it >> 1) & 1;
+      const uint32_t acc_ph = it & 1;
       ++it;
-      if (!tc::mbar_wait(&tmem_empty[acc], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
+      // Both accumulators free (the epilogue of the previous tile has read them).
+      if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma) ||
             !tc::mbar_wait(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
@@ -367,9 +374,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           const uint32_t b_addr = smem_base + L::kDeqOff + d * kDeqBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t ad = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
             const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
-            tc::mma_bf16(d_tmem, ad, bd, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t a0 = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
+            const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
+            tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
           }
           tc::mma_commit(&empty_raw[s]);
           tc::mma_commit(&empty_deq[d]);
@@ -379,7 +389,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         if (++d == kDeqStages) { d = 0; dph ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) tc::mma_commit(&tmem_full[acc]);
+      if (lane == 0) tc::mma_commit(&tmem_full[0]);
       __syncwarp();
     }
     // Drain: every MMA issued by this thread completes before TMEM is freed.
@@ -445,16 +455,16 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   } else if (warp >= kEpiWarp0) {
     // --------------------------------------------------------- epilogue --
     const int g = warp & 3;                 // TMEM lane group of this warp
-    const int r_local = g * 32 + lane;      // accumulator row (tile-local)
     int it = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid) continue;
-      const int m = tl.m0 + r_local;
-      const bool row_ok = m < tl.m_end;
       if (tl.expert < 0) {
         // Inactive group: write zeros for its rows, no tensor-core work.
-        if (row_ok) {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
+          if (m >= tl.m_end) continue;
           for (int c = 0; c < BN && tl.n0 + c < p.N; ++c) {
             const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0 + c;
             if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
@@ -463,47 +473,54 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         continue;
       }
-      const int acc = it & 1;
-      const uint32_t acc_ph = (it >> 1) & 1;
+      const uint32_t acc_ph = it & 1;
       ++it;
-      if (!tc::mbar_wait(&tmem_full[acc], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
+      if (!tc::mbar_wait(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
       tc::tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + acc * BN;
       const bool vec_ok = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld_32x32b_x32(taddr + c0, r);
-        tc::tmem_wait_ld();
-        const int n = tl.n0 + c0;
-        if (!row_ok || n >= p.N) continue;
-        float v[32];
+      for (int h = 0; h < 2; ++h) {
+        const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
+        const bool row_ok = m < tl.m_end;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(taddr + c0, r);
+          tc::tmem_wait_ld();
+          const int n = tl.n0 + c0;
+          if (!row_ok || n >= p.N) continue;
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
-        const int64_t o = static_cast<int64_t>(m) * p.N + n;
-        if (vec_ok && n + 32 <= p.N) {
-          if (p.bf16_out) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
+          for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+          const int64_t o = static_cast<int64_t>(m) * p.N + n;
+          if (vec_ok && n + 32 <= p.N) {
+            if (p.bf16_out) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
           } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+            const int lim = min(32, p.N - n);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
-        } else {
-          const int lim = min(32, p.N - n);
-          for (int i = 0; i < lim; ++i) {
-            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + i] = __float2bfloat16_rn(v[i]);
-            else static_cast<float*>(p.out)[o + i] = v[i];
+            for (int i = 0; i < 32; ++i) {
+              if (i < lim) {
+                if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + i] = __float2bfloat16_rn(v[i]);
+                else static_cast<float*>(p.out)[o + i] = v[i];
+              }
+            }
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tmem_empty[acc]);
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
     }
   }
 

@@ -88,59 +88,6 @@ __device__ __forceinline__ void load_w8(const uint8_t* __restrict__ p, uint32_t*
   }
 }
 
-// Two e4m3 codes in each half of a 32-bit word -> two f16x2 (hardware cvt,
-// exact); the half selection is part of the instruction.
-__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
-// f16x2 -> (f32, f32).
-__device__ __forceinline__ float2 h2f2(uint32_t h) {
-  float a, b;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-      : "=f"(a), "=f"(b)
-      : "r"(h));
-  return make_float2(a, b);
-}
-
-// acc += a * b on both halves: one packed fp32 FMA (fma.rn.f32x2).
-__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(r)
-      : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
-        "l"(*reinterpret_cast<unsigned long long*>(&acc)));
-  acc = *reinterpret_cast<float2*>(&r);
-}
-
-// bf16x2 bit patterns -> (f32, f32), exact.
-__device__ __forceinline__ float2 bf2f2(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
-
-// Byte B (0..3) of a word holds two E2M1 codes -> f16x2 (hardware cvt, exact).
-template <int B>
-__device__ __forceinline__ uint32_t e2m1x2_b(uint32_t w) {
-  uint32_t out;
-  if constexpr (B == 0) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
-        : "=r"(out) : "r"(w));
-  } else if constexpr (B == 1) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
-        : "=r"(out) : "r"(w));
-  } else if constexpr (B == 2) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
-        : "=r"(out) : "r"(w));
-  } else {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
-        : "=r"(out) : "r"(w));
-  }
-  return out;
-}
-
 // 16 fp8 codes (4 words) x 16 activations (8 f32 pairs) into a pair
 // accumulator: 8 cvt, 8 x 2 cvt.f32.f16 and 8 packed FMAs.
 __device__ __forceinline__ void dot16_fp8(const uint32_t* w, const float2* xf, float2& acc) {
