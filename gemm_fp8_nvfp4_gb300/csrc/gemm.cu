@@ -54,6 +54,7 @@ constexpr int BN = 256;          // weight rows per tile (MMA N)
 constexpr int BK = 64;           // K per stage (one 128-byte swizzle row of bf16)
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
 constexpr int kRawStages = 3;
+constexpr int kL2Prefetch = 8;   // weight tiles prefetched into L2 this many K steps ahead
 constexpr int kDeqStages = 2;
 constexpr int kThreads = 512;    // 16 warps
 constexpr int kWarpTma = 0;
@@ -297,10 +298,34 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    // Weight tiles are prefetched into L2 kL2Prefetch K steps ahead (into the
+    // CTA's next tile near the end of a tile): the ring holds only a few
+    // stages, too few to hide DRAM latency when the weight is not yet in L2
+    // (grouped: every expert's weight streams from DRAM once).
+    auto prefetch_w = [&](const Tile& pt, int pkb) {
+      if (lane != 0 || !pt.valid || pt.expert < 0) return;
+      if constexpr (F == Fmt::kFp8) {
+        if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * BK, pt.n0, pt.expert);
+        else tc::tma_prefetch_l2_2d(&tmap_w, pkb * BK, pt.n0);
+      } else {
+        tc::tma_prefetch_l2_2d(&tmap_w, pkb * (BK / 2), pt.n0);
+      }
+    };
+    {
+      const Tile first = blockIdx.x < total_tiles ? get_tile<kGrouped>(p, blockIdx.x) : Tile{};
+      if (blockIdx.x < total_tiles)
+        for (int kb = 0; kb < kL2Prefetch && kb < nkb; ++kb) prefetch_w(first, kb);
+    }
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
+      const int tn = t + static_cast<int>(gridDim.x);
+      Tile next{};
+      next.valid = false;
+      if (tn < total_tiles) next = get_tile<kGrouped>(p, tn);
       for (int kb = 0; kb < nkb; ++kb) {
+        if (kb + kL2Prefetch < nkb) prefetch_w(tl, kb + kL2Prefetch);
+        else if (kb + kL2Prefetch - nkb < nkb) prefetch_w(next, kb + kL2Prefetch - nkb);
         if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
@@ -359,6 +384,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       if (!tl.valid || tl.expert < 0) continue;
       const uint32_t acc_ph = it & 1;
       ++it;
+      const bool two_halves = tl.m_end - tl.m0 > UMMA_M;
       // Both accumulators free (the epilogue of the previous tile has read them).
       if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
@@ -379,7 +405,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
-            tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
+            // A tile with at most 128 rows (ragged end of M or of a group)
+            // needs only the first half; the second accumulator is unused.
+            if (two_halves) tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
           }
           tc::mma_commit(&empty_raw[s]);
           tc::mma_commit(&empty_deq[d]);
@@ -461,14 +489,23 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       if (!tl.valid) continue;
       if (tl.expert < 0) {
         // Inactive group: write zeros for its rows, no tensor-core work.
+        const bool vec0 = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
+        const int per16 = p.bf16_out ? 8 : 4;            // elements per 16-byte store
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
           if (m >= tl.m_end) continue;
-          for (int c = 0; c < BN && tl.n0 + c < p.N; ++c) {
-            const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0 + c;
-            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
-            else static_cast<float*>(p.out)[o] = 0.f;
+          const int cend = min(BN, p.N - tl.n0);
+          const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0;
+          int c = 0;
+          if (vec0) {
+            uint4* dst = p.bf16_out ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o)
+                                    : reinterpret_cast<uint4*>(static_cast<float*>(p.out) + o);
+            for (; c + per16 <= cend; c += per16) dst[c / per16] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          for (; c < cend; ++c) {
+            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + c] = __float2bfloat16_rn(0.f);
+            else static_cast<float*>(p.out)[o + c] = 0.f;
           }
         }
         continue;
@@ -478,8 +515,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       if (!tc::mbar_wait(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
       tc::tc_fence_after();
       const bool vec_ok = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
+      const int halves = tl.m_end - tl.m0 > UMMA_M ? 2 : 1;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < halves; ++h) {
         const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
