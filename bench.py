@@ -265,6 +265,8 @@ def run_ours(args, rank, local, world):
             gq.fp8_gemv(x, w, s, out=outs[j], stream=stream)
 
     sampler = ClockSampler(local)
+    if args.overlap_weight_reads:
+        gq.set_launch_flags(gq.GQ_LAUNCH_OVERLAP_WEIGHT_READS)
     ms = graph_timer(gemv_step, args.steps, args.warmup, min(200, args.steps), stream, world,
                      sampler)
     gemv_launches = 3 * args.steps
@@ -294,6 +296,8 @@ def run_ours(args, rank, local, world):
             "l2": f"inputs larger than L2: {copies} rotating weight copies "
                   f"({copies * sum(n * k for n, k in GEMV_SHAPES) / 1e6:.0f} MB per rotation)",
             "timing": "CUDA-graph replay, CUDA events on the launching stream",
+            "launch": ("GQ_LAUNCH_OVERLAP_WEIGHT_READS (weight reads overlap the previous GEMV)"
+                       if args.overlap_weight_reads else "plain stream order"),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roofline": {
@@ -311,6 +315,19 @@ def run_ours(args, rank, local, world):
         "clocks": clocks,
     }
 
+    if not args.overlap_weight_reads and not args.headline_only:
+        # The same step with GQ_LAUNCH_OVERLAP_WEIGHT_READS (decode with fixed
+        # weights: each GEMV's weight reads overlap the previous kernel).
+        gq.set_launch_flags(gq.GQ_LAUNCH_OVERLAP_WEIGHT_READS)
+        ms_o = graph_timer(gemv_step, args.steps, args.warmup, min(200, args.steps), stream, world)
+        gq.set_launch_flags(0)
+        tb_o, ms_o = aggregate(world, step_bytes * args.steps, ms_o, device=dev)
+        v_o = tb_o / (ms_o * 1e-3) / 1e9
+        line["overlap_weight_reads"] = {
+            "value": round(v_o, 1), "unit": "GB/s", "ms_per_step": ms_o / args.steps,
+            "frac": round(v_o / world / peaks["hbm_gbs"], 4),
+            "note": "same step with GQ_LAUNCH_OVERLAP_WEIGHT_READS: valid when no kernel "
+                    "between GEMVs writes their weights (decode with fixed weights)"}
     if not args.headline_only:
         line["sub"] = run_subs(args, gq, dev, stream, peaks, world)
         line["gpu_launches"] = gemv_launches  # the timed region of the headline only
@@ -578,6 +595,9 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the FP8 GEMV headline (no sub-benchmarks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap-weight-reads", action="store_true",
+                    help="GEMVs overlap their weight reads with the previous kernel "
+                         "(GQ_LAUNCH_OVERLAP_WEIGHT_READS; weights are not written between launches)")
     ap.add_argument("--only", choices=["nvfp4", "gemm", "grouped", "gemv-shapes"], default=None,
                     help="run one sub-benchmark alone and print its result (for profiling)")
     args = ap.parse_args()
@@ -620,6 +640,8 @@ def run_only(args, local):
     dev = torch.device("cuda", local)
     gq.load_library()
     stream = torch.cuda.Stream(device=dev)
+    if args.overlap_weight_reads:
+        gq.set_launch_flags(gq.GQ_LAUNCH_OVERLAP_WEIGHT_READS)
     if args.only == "gemv-shapes":
         print(json.dumps({"only": args.only,
                           "shapes": gemv_shape_times(gq, dev, stream, args.steps, args.warmup)}),

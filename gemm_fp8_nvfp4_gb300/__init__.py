@@ -41,7 +41,11 @@ SIGNATURES = {
     "gq_fp8_materialize": (_I, [_P, _I, _P, _I64, _I64, _P]),
     "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
+    "gq_set_launch_flags": (_I, [ctypes.c_uint32]),
+    "gq_get_launch_flags": (ctypes.c_uint32, []),
 }
+
+GQ_LAUNCH_OVERLAP_WEIGHT_READS = 1
 
 
 class GQError(RuntimeError):
@@ -243,6 +247,17 @@ def nvfp4_materialize(q, bs, out=None, out_dtype=torch.bfloat16, stream=None):
     return o
 
 
+def set_launch_flags(flags: int) -> None:
+    """Process-wide launch options; GQ_LAUNCH_OVERLAP_WEIGHT_READS lets a GEMV's
+    weight reads overlap the previous kernel in the stream (see include/gq.h:
+    only when that kernel does not write the weights)."""
+    _check(load_library().gq_set_launch_flags(int(flags)), "set_launch_flags")
+
+
+def get_launch_flags() -> int:
+    return int(load_library().gq_get_launch_flags())
+
+
 def device_status(reset: bool = False) -> int:
     """Status flags recorded by bounded in-kernel waits that ran out (synchronizes)."""
     v = ctypes.c_uint32(0)
@@ -253,5 +268,6 @@ def device_status(reset: bool = False) -> int:
 __all__ = [
     "fp8_gemv", "nvfp4_gemv", "fp8_matmul", "nvfp4_matmul", "fp8_grouped_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
+    "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
     "SIGNATURES", "LIB_PATH", "version", "status_str",
 ]

@@ -29,6 +29,7 @@ struct DeviceInfo {
 };
 
 DeviceInfo g_devices[kMaxDevices];
+std::atomic<uint32_t> g_launch_flags{0};
 
 // Fills `ctx` for the current device; returns GQ_OK or GQ_ERR_DEVICE.
 int device_ctx(cudaStream_t stream, Ctx* ctx) {
@@ -62,6 +63,8 @@ int device_ctx(cudaStream_t stream, Ctx* ctx) {
   ctx->status = d.status;
   ctx->num_sms = d.num_sms;
   ctx->device = dev;
+  ctx->overlap_weights =
+      (g_launch_flags.load(std::memory_order_relaxed) & GQ_LAUNCH_OVERLAP_WEIGHT_READS) != 0;
   return GQ_OK;
 }
 
@@ -117,6 +120,14 @@ const char* gq_status_str(int s) {
 }
 
 const char* gq_version(void) { return "gq 0.1.0 sm_103a"; }
+
+int gq_set_launch_flags(uint32_t flags) {
+  if (flags & ~static_cast<uint32_t>(GQ_LAUNCH_OVERLAP_WEIGHT_READS)) return GQ_ERR_SHAPE;
+  gq::g_launch_flags.store(flags, std::memory_order_relaxed);
+  return GQ_OK;
+}
+
+uint32_t gq_get_launch_flags(void) { return gq::g_launch_flags.load(std::memory_order_relaxed); }
 
 int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w, int64_t N,
                 int64_t K, float alpha, cudaStream_t stream) {

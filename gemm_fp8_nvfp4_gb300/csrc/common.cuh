@@ -178,6 +178,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Programmatic dependent launch.  pdl_wait() blocks until the grid this one
+// depends on (the previous kernel in the stream, when this kernel was launched
+// with programmatic stream serialization) has completed and its memory is
+// visible; without such a dependency it returns at once.  Every access to
+// memory that the previous kernel may write must come after it.
+// pdl_launch_dependents() lets the next kernel start launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The same wait without a compiler memory clobber, for kernels whose global
+// loads are all volatile asm (never moved across it) and whose stores depend
+// on data loaded after it; it keeps register allocation unconstrained.
+__device__ __forceinline__ void pdl_wait_ordered() { asm volatile("griddepcontrol.wait;"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t bit) {
   if (status != nullptr) atomicOr(status, bit);
 }

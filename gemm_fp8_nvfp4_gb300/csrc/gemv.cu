@@ -20,6 +20,13 @@
 // Weight loads bypass L1 (read once); activation loads go through L1 because
 // every CTA on the SM reads the same x.
 //
+// With GQ_LAUNCH_OVERLAP_WEIGHT_READS the GEMV is launched as a programmatic
+// dependent of the previous kernel in the stream: each thread issues its first
+// batch of weight loads, then waits (griddepcontrol.wait) for that kernel to
+// complete before it reads x or writes y.  The weight stream of one GEMV thus overlaps the tail
+// of the previous kernel -- valid only when that kernel does not write the
+// weights, which is why it is opt-in.
+//
 // The load width adapts to K and the pointers: 16 bytes when K % 16 == 0,
 // down to 1 byte for odd K (the pages' scalar tail for K % TILE_K != 0 becomes
 // a narrower vector for the whole row, so no row ever straddles an unaligned
@@ -33,6 +40,7 @@ namespace {
 constexpr int kThreads = 128;   // threads per CTA (8 CTAs fit on an SM)
 
 // ---------------------------------------------------------------- helpers --
+
 
 // Load VEC bf16 activations starting at element k0 and widen to f32.
 template <int VEC>
@@ -156,14 +164,19 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
 
 // ------------------------------------------------------------------- FP8 --
 
-template <int VEC, int R, int U, int T = kThreads>
-__global__ void __launch_bounds__(T)
+template <int VEC, int R, int U, int T = kThreads, bool kOverlap = false>
+__global__ void __launch_bounds__(T, 7)   // 7 CTAs per SM (<= 73 registers)
 k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
            const uint8_t* __restrict__ w, int64_t N, int64_t K, float alpha) {
   constexpr int kThreads = T;
   __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t nvec = K / VEC;
+  // Overlap mode: the first batch of weight loads is issued before the wait
+  // for the previous kernel; x is read and y written only after it.
+  if constexpr (kOverlap) pdl_launch_dependents();
+  if constexpr (kOverlap && VEC != 16) pdl_wait_ordered();
+  bool waited = !kOverlap || VEC != 16;
   constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
 
   // Rows past N (last CTA) re-read the last valid row and are never stored.
@@ -188,6 +201,10 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int r = 0; r < R; ++r) wv[u][r] = ld_stream_v4(rows[r] + (v + u * kThreads) * 16);
+      if (!waited) {
+        pdl_wait_ordered();
+        waited = true;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint4 xa = ld_ro_v4(x + (v + u * kThreads) * 16);
@@ -205,6 +222,10 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       uint4 wv[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) wv[r] = ld_stream_v4(rows[r] + v * 16);
+      if (!waited) {
+        pdl_wait_ordered();
+        waited = true;
+      }
       const uint4 xa = ld_ro_v4(x + v * 16);
       const uint4 xb = ld_ro_v4(x + v * 16 + 8);
       const float2 xf[8] = {bf2f2(xa.x), bf2f2(xa.y), bf2f2(xa.z), bf2f2(xa.w),
@@ -245,6 +266,7 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       for (int r = 0; r < R; ++r) acc[r] = fma_fp8<VEC>(wv[r], xf, acc[r]);
     }
   }
+  if (!waited) pdl_wait_ordered();   // threads without a vector still order their store
   reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
 }
 
@@ -284,8 +306,8 @@ __device__ __forceinline__ void load_xf(const uint16_t* __restrict__ x, int64_t 
   }
 }
 
-template <int VB, int R, int U, int T = kThreads>
-__global__ void __launch_bounds__(T)
+template <int VB, int R, int U, int T = kThreads, bool kOverlap = false>
+__global__ void __launch_bounds__(T, 6)   // 6 CTAs per SM (<= 85 registers)
 k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
              const uint8_t* __restrict__ q, const uint8_t* __restrict__ bs, int64_t N,
              int64_t K, float alpha) {
@@ -293,6 +315,8 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
   __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t half_k = K / 2;
+  if constexpr (kOverlap) pdl_launch_dependents();
+  bool waited = !kOverlap;
   const int64_t nvec = half_k / VB;
   constexpr int kWords = VB / 4;
   constexpr int kBlocks = VB / 8;
@@ -326,6 +350,10 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
         load_w8<VB>(qrows[r] + (v + u * kThreads) * VB, wv[u][r]);
         sv[u][r] = load_scales(srows[r], v + u * kThreads);
       }
+    if (!waited) {
+      pdl_wait_ordered();
+      waited = true;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       float2 xf[VB];
@@ -342,6 +370,10 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
       load_w8<VB>(qrows[r] + v * VB, wv[r]);
       sv[r] = load_scales(srows[r], v);
     }
+    if (!waited) {
+      pdl_wait_ordered();
+      waited = true;
+    }
     float2 xf[VB];
     load_xf<VB>(x, v * 2 * VB, xf);
 #pragma unroll
@@ -350,6 +382,7 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = acc2[r].x + acc2[r].y;
+  if (!waited) pdl_wait_ordered();   // threads without a vector still order their store
   reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
 }
 
@@ -360,9 +393,14 @@ cudaError_t fp8_dispatch(const Ctx& c, void* y, bool bf16_out, const void* x,
                          const uint8_t* w, int64_t N, int64_t K, float alpha) {
   const int64_t grid = (N + kRows - 1) / kRows;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
-      y, bf16_out, static_cast<const uint16_t*>(x), w, N, K, alpha);
-  return cudaGetLastError();
+  if (c.overlap_weights) {
+    return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2), kThreads, true>,
+                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
+                         static_cast<const uint16_t*>(x), w, N, K, alpha);
+  }
+  return launch_kernel(c, false, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)>,
+                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
+                       static_cast<const uint16_t*>(x), w, N, K, alpha);
 }
 
 }  // namespace
@@ -384,18 +422,32 @@ cudaError_t launch_fp8_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
 cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
                               const uint8_t* q, const uint8_t* bs, int64_t N,
                               int64_t K, float alpha) {
-  const int64_t grid = (N + kRows - 1) / kRows;
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   const bool wide = (K % 32 == 0) && (reinterpret_cast<uintptr_t>(bs) % 2 == 0);
   if (wide) {
-    k_nvfp4_gemv<16, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
-        y, bf16_out, xb, q, bs, N, K, alpha);
-  } else {
-    k_nvfp4_gemv<8, kRows, 2><<<static_cast<unsigned>(grid), kThreads, 0, c.stream>>>(
-        y, bf16_out, xb, q, bs, N, K, alpha);
+    // 8 rows per CTA, one 16-byte vector per row per step (best at N = K = 4096).
+    constexpr int kRowsWide = 8;
+    const int64_t grid = (N + kRowsWide - 1) / kRowsWide;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (c.overlap_weights) {
+      return launch_kernel(c, true, k_nvfp4_gemv<16, kRowsWide, 1, kThreads, true>,
+                           dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb,
+                           q, bs, N, K, alpha);
+    }
+    return launch_kernel(c, false, k_nvfp4_gemv<16, kRowsWide, 1>,
+                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
+                         bs, N, K, alpha);
   }
-  return cudaGetLastError();
+  const int64_t grid = (N + kRows - 1) / kRows;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (c.overlap_weights) {
+    return launch_kernel(c, true, k_nvfp4_gemv<8, kRows, 2, kThreads, true>,
+                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
+                         bs, N, K, alpha);
+  }
+  return launch_kernel(c, false, k_nvfp4_gemv<8, kRows, 2>,
+                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
+                       bs, N, K, alpha);
 }
 
 }  // namespace gq

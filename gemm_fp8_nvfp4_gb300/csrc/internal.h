@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 namespace gq {
@@ -13,7 +15,28 @@ struct Ctx {
   uint32_t* status;   // device address of the per-device status word
   int num_sms;        // multiprocessor count of the current device
   int device;
+  bool overlap_weights;  // GQ_LAUNCH_OVERLAP_WEIGHT_READS is set (gq_set_launch_flags)
 };
+
+// Launch `kern` on c.stream.  With `pdl` the launch carries the programmatic
+// stream serialization attribute: the kernel may start before the previous
+// kernel in the stream finishes and must call pdl_wait() before touching
+// memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const Ctx& c, bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                          size_t smem, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // materialize.cu
 cudaError_t launch_fp8_materialize(const Ctx& c, void* out, bool bf16_out,

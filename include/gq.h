@@ -63,6 +63,25 @@ typedef enum {
 
 typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
 
+/*
+ * Process-wide launch options (default 0).
+ *
+ * GQ_LAUNCH_OVERLAP_WEIGHT_READS: the GEMV entry points (gq_fp8_gemv,
+ * gq_nvfp4_gemv) launch their kernel as a programmatic dependent of the
+ * previous kernel in the stream.  Each thread issues its first weight loads
+ * immediately and waits for the previous kernel to finish (and its writes to
+ * become visible) before it reads x or writes y.  The weight stream of a GEMV
+ * then overlaps the tail of the kernel before it, which is what a decode loop
+ * over layers with fixed weights wants.  Only set it when no kernel issued
+ * just before a GEMV writes that GEMV's weight buffers: those reads are not
+ * ordered after the previous kernel.  Activations and outputs always are.
+ * Not a citation of the pages: a GB300 launch option.
+ * gq_set_launch_flags returns GQ_ERR_SHAPE for unknown bits.
+ */
+#define GQ_LAUNCH_OVERLAP_WEIGHT_READS 1u
+int gq_set_launch_flags(uint32_t flags);
+uint32_t gq_get_launch_flags(void);
+
 /* Human-readable name of a gq_status value (static string). */
 const char* gq_status_str(int status);
 

@@ -168,3 +168,64 @@ def test_gemv_row_splits(n, k):
     run_fp8(n, k, torch.float32, seed=n)
     if k % 32 == 0:
         run_nvfp4(n, k, torch.float32, seed=n + 1)
+
+
+@pytest.fixture
+def overlap_flag():
+    """GQ_LAUNCH_OVERLAP_WEIGHT_READS on for the test, restored afterwards."""
+    lib()
+    old = gq.get_launch_flags()
+    gq.set_launch_flags(gq.GQ_LAUNCH_OVERLAP_WEIGHT_READS)
+    yield
+    gq.set_launch_flags(old)
+
+
+def test_overlap_flag_gives_identical_results(overlap_flag):
+    codes, scale = synth.fp8_weight(1000, 4096, seed=21)
+    q, bs, s2 = synth.nvfp4_weight(1000, 4096, seed=22)
+    x = synth.bf16_activations(1, 4096, seed=23).reshape(-1).to(DEV)
+    w, qd, bsd = codes.to(DEV), q.to(DEV), bs.to(DEV)
+    on8 = gq.fp8_gemv(x, w, scale, out_dtype=torch.float32)
+    on4 = gq.nvfp4_gemv(x, qd, bsd, s2, out_dtype=torch.float32)
+    gq.set_launch_flags(0)
+    off8 = gq.fp8_gemv(x, w, scale, out_dtype=torch.float32)
+    off4 = gq.nvfp4_gemv(x, qd, bsd, s2, out_dtype=torch.float32)
+    assert torch.equal(on8, off8) and torch.equal(on4, off4)
+
+
+def test_overlap_flag_orders_activation_reads(overlap_flag):
+    """A chain of dependent GEMVs (the output of one is the input of the next)
+    and a torch kernel writing x right before a GEMV: with the overlap flag
+    every x read still sees the previous kernel's result."""
+    n = 4096
+    codes = [synth.fp8_weight(n, n, seed=30 + i)[0] for i in range(3)]
+    ws = [c.to(DEV) for c in codes]
+    x0 = synth.bf16_activations(1, n, seed=40).reshape(-1)
+    xs = x0.to(DEV)
+    outs = []
+    for i in range(3):
+        y = gq.fp8_gemv(xs, ws[i], 0.02, out_dtype=torch.bfloat16)
+        outs.append(y)
+        xs = y
+    # torch writes x in place, then a GEMV reads it
+    xt = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    xt.copy_(x0.to(DEV))
+    yt = gq.fp8_gemv(xt, ws[0], 0.02, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    # reference chain on the oracle, each step from the GPU's bf16 input
+    xin = bits(x0)
+    for i in range(3):
+        ref = oracle.fp8_gemv(xin, codes[i].numpy(), 0.02)
+        tol = oracle.tolerance(xin[None, :], oracle.decode_fp8(codes[i].numpy()), 0.02, True,
+                               ref=ref[None, :])[0]
+        assert_within(to_f64(outs[i]), ref, tol, f"chain step {i}")
+        xin = bits(outs[i].cpu())
+    ref = oracle.fp8_gemv(bits(x0), codes[0].numpy(), 0.02)
+    assert_within(to_f64(yt), ref, oracle.tolerance(bits(x0)[None, :],
+                  oracle.decode_fp8(codes[0].numpy()), 0.02)[0], "after torch write")
+
+
+def test_launch_flags_reject_unknown_bits():
+    lib()
+    with pytest.raises(gq.GQError):
+        gq.set_launch_flags(0x80)
