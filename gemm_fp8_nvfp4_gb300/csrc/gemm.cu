@@ -64,6 +64,7 @@ constexpr int kDeqWarps = 8;     // 256 threads: one weight row each
 constexpr int kEpiWarp0 = 12;    // 4 warps: TMEM lane groups 0..3
 constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators (one per A half)
 
+constexpr uint32_t kPartStride = BN * 4 + 16;   // split-K partial row: 256 fp32 + pad
 constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
 constexpr uint32_t kAHalfBytes = UMMA_M * BK * 2;  // 16 KB: offset of the second A half
 constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
@@ -94,6 +95,10 @@ template <Fmt F> struct Smem {
   static constexpr uint32_t kAlloc = kTotal + 1024;              // slack for 1 KB alignment
 };
 
+static_assert(UMMA_M * kPartStride <= Smem<Fmt::kNvfp4>::kBarOff &&
+                  UMMA_M * kPartStride <= Smem<Fmt::kFp8>::kBarOff,
+              "split-K partials fit below the barriers");
+
 // Work description shared by the plain and grouped GEMMs.
 struct Problem {
   void* out;
@@ -107,6 +112,8 @@ struct Problem {
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
   int bf16_out;
+  int ksplit;                  // > 1: split-K over a thread-block cluster of ksplit CTAs
+  int kb_per_split;            // K steps per split
 };
 
 // A tile of work: rows [m0, m_end) of C, columns [n0, n0 + BN), weight index.
@@ -291,7 +298,15 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const uint32_t tmem_base = *tmem_slot;
 
   const int total_tiles = num_tiles<kGrouped>(p);
-  const int nkb = p.num_k_blocks;
+  // Split-K (small M): the CTAs of a cluster share one tile, rank r owns the
+  // K steps [kb0, kb1); otherwise a CTA walks tiles persistently over all K.
+  const bool split = p.ksplit > 1;
+  const int crank = split ? static_cast<int>(blockIdx.x) % p.ksplit : 0;
+  const int t_first = split ? static_cast<int>(blockIdx.x) / p.ksplit : static_cast<int>(blockIdx.x);
+  const int t_step = split ? total_tiles : static_cast<int>(gridDim.x);
+  const int kb0 = split ? crank * p.kb_per_split : 0;
+  const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
+  const int nkb = kb1;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer --
@@ -311,21 +326,20 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         tc::tma_prefetch_l2_2d(&tmap_w, pkb * (BK / 2), pt.n0);
       }
     };
-    {
-      const Tile first = blockIdx.x < total_tiles ? get_tile<kGrouped>(p, blockIdx.x) : Tile{};
-      if (blockIdx.x < total_tiles)
-        for (int kb = 0; kb < kL2Prefetch && kb < nkb; ++kb) prefetch_w(first, kb);
+    if (t_first < total_tiles) {
+      const Tile first = get_tile<kGrouped>(p, t_first);
+      for (int kb = kb0; kb < kb0 + kL2Prefetch && kb < nkb; ++kb) prefetch_w(first, kb);
     }
-    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < total_tiles && ok; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
-      const int tn = t + static_cast<int>(gridDim.x);
+      const int tn = t + t_step;
       Tile next{};
       next.valid = false;
       if (tn < total_tiles) next = get_tile<kGrouped>(p, tn);
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb0; kb < nkb; ++kb) {
         if (kb + kL2Prefetch < nkb) prefetch_w(tl, kb + kL2Prefetch);
-        else if (kb + kL2Prefetch - nkb < nkb) prefetch_w(next, kb + kL2Prefetch - nkb);
+        else if (kb + kL2Prefetch - nkb < nkb && !split) prefetch_w(next, kb + kL2Prefetch - nkb);
         if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
@@ -379,7 +393,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     uint32_t ph = 0, dph = 0;
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < total_tiles && ok; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
       const uint32_t acc_ph = it & 1;
@@ -388,7 +402,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       // Both accumulators free (the epilogue of the previous tile has read them).
       if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma) ||
             !tc::mbar_wait(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
           ok = false;
@@ -403,7 +417,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
             const uint64_t a0 = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
             const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
-            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
             tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
             // A tile with at most 128 rows (ragged end of M or of a group)
             // needs only the first half; the second accumulator is unused.
@@ -432,10 +446,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < total_tiles && ok; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant) ||
             !tc::mbar_wait(&empty_deq[d], dph ^ 1, abort_flag, p.status, kStatusTimeoutDequant)) {
           ok = false;
@@ -484,7 +498,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // --------------------------------------------------------- epilogue --
     const int g = warp & 3;                 // TMEM lane group of this warp
     int it = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    for (int t = t_first; t < total_tiles; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid) continue;
       if (tl.expert < 0) {
@@ -514,6 +528,30 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       ++it;
       if (!tc::mbar_wait(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
       tc::tc_fence_after();
+      if (split) {
+        // This CTA's raw fp32 partial of rows [0, 128) -> shared memory (the
+        // operand rings are idle now: every MMA has completed).  Rows are
+        // padded to kPartStride bytes so that 8 consecutive rows hit
+        // distinct banks.  The cluster reduction at the end of the kernel sums
+        // the partials of all ranks.
+        const int r_local = g * 32 + lane;
+        const uint32_t prow = smem_base + r_local * kPartStride;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + c0, r);
+          tc::tmem_wait_ld();
+          if (tl.m0 + r_local < tl.m_end) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              tc::sts128(prow + (c0 + 4 * i) * 4, make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]));
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
+        continue;
+      }
       const bool vec_ok = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
       const int halves = tl.m_end - tl.m0 > UMMA_M ? 2 : 1;
 #pragma unroll 1
@@ -564,6 +602,41 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
 
   tc::tc_fence_before();
   __syncthreads();
+  if (split) {
+    // Split-K reduction across the cluster through distributed shared
+    // memory: rank r sums columns [r * BN / S, (r + 1) * BN / S) of the tile
+    // over all ranks in rank order (deterministic), scales, converts, stores.
+    tc::cluster_sync();
+    if (t_first < total_tiles) {
+      const Tile tl = get_tile<kGrouped>(p, t_first);
+      const int rows = tl.m_end - tl.m0;
+      const int cols = BN / p.ksplit;                 // multiple of 4 (host check)
+      const int c_begin = crank * cols;
+      const int groups = rows * (cols / 4);
+      for (int task = threadIdx.x; task < groups; task += kThreads) {
+        const int r = task / (cols / 4);
+        const int c = c_begin + 4 * (task % (cols / 4));
+        const uint32_t local = smem_base + r * kPartStride + c * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < p.ksplit; ++q) {
+          const float4 v = tc::ld_cluster_f4(tc::map_to_rank(local, q));
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const int m = tl.m0 + r;
+        const int n = tl.n0 + c;
+        const float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        const int64_t base = static_cast<int64_t>(m) * p.N + n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (n + i < p.N) {
+            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[base + i] = __float2bfloat16_rn(o[i]);
+            else static_cast<float*>(p.out)[base + i] = o[i];
+          }
+        }
+      }
+    }
+    tc::cluster_sync();   // no CTA leaves while a peer still reads its partial
+  }
   if (warp == kWarpMma) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, kTmemCols);
@@ -622,8 +695,19 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kern<<<grid, kThreads, smem, c.stream>>>(ta, tw, scales, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.ksplit > 1 ? p.ksplit : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.ksplit > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, scales, p);
 }
 
 cudaError_t fill_zero(const Ctx& c, void* out, bool bf16_out, int64_t count, float alpha) {
@@ -644,7 +728,26 @@ Problem base_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_t 
   p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
   p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
   p.bf16_out = bf16_out ? 1 : 0;
+  p.ksplit = 1;
+  p.kb_per_split = p.num_k_blocks;
   return p;
+}
+
+// Small M: too few tiles to fill the GPU.  Split K over a cluster of up to 4
+// CTAs (clusters of 8 one-CTA-per-SM blocks do not all fit in one wave) when each tile has at most 128 rows (one MMA half; the partials fit in
+// shared memory) and every split gets at least 4 K steps.  Returns the grid.
+int plan_split(const Ctx& c, Problem& p, int tiles) {
+  if (p.M > UMMA_M || tiles * 2 > c.num_sms) return std::min(tiles, c.num_sms);
+  int s = std::min(4, c.num_sms / tiles);
+  s = std::min(s, p.num_k_blocks / 4);
+  while (s > 1 && (BN / s) % 4 != 0) --s;
+  if (s < 2) return std::min(tiles, c.num_sms);
+  const int per = (p.num_k_blocks + s - 1) / s;
+  s = (p.num_k_blocks + per - 1) / per;           // no empty split
+  if (s < 2 || (BN / s) % 4 != 0) return std::min(tiles, c.num_sms);
+  p.ksplit = s;
+  p.kb_per_split = per;
+  return tiles * s;
 }
 
 }  // namespace
@@ -659,7 +762,8 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* 
     return cudaErrorInvalidValue;
   Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
-  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, std::min(tiles, c.num_sms));
+  const int grid = plan_split(c, p, tiles);
+  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, grid);
 }
 
 cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
@@ -674,7 +778,8 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void
     return cudaErrorInvalidValue;
   Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
-  return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, std::min(tiles, c.num_sms));
+  const int grid = plan_split(c, p, tiles);
+  return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid);
 }
 
 cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,

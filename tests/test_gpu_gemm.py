@@ -172,3 +172,25 @@ def test_no_wait_timed_out():
     lib()
     torch.cuda.synchronize()
     assert gq.device_status() == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 4096, 4096), (128, 1000, 4112), (100, 520, 2048),
+                                   (128, 4096, 1024)])
+def test_small_m_split_k(m, n, k):
+    """M <= 128 with few N tiles: K is split over a thread-block cluster and
+    the partials are reduced through distributed shared memory (ragged last
+    split for K = 4112, N not a multiple of the tile)."""
+    lib()
+    check_fp8(m, n, k, seed=m + k)
+    if k % 64 == 0:
+        check_nvfp4(m, n, k, seed=m + k + 1)
+
+
+def test_small_m_split_k_deterministic():
+    lib()
+    codes, s = synth.fp8_weight(4096, 4096, seed=50)
+    a = synth.bf16_activations(64, 4096, seed=51).to(DEV)
+    w = codes.to(DEV)
+    r1 = gq.fp8_matmul(a, w, s, out_dtype=torch.float32)
+    r2 = gq.fp8_matmul(a, w, s, out_dtype=torch.float32)
+    assert torch.equal(r1, r2)

@@ -92,9 +92,13 @@ def test_grouped_equals_dense_per_group():
     offs, ids = [0, 100, 260], [1, 0]
     got = run_grouped(a, stack, scales, offs, ids, max_rows=160)
     for z, e in enumerate(ids):
-        dense = to_f64(gq.fp8_matmul(a[offs[z]:offs[z + 1]].to(DEV), stack[e].to(DEV),
+        rows = a[offs[z]:offs[z + 1]]
+        dense = to_f64(gq.fp8_matmul(rows.to(DEV), stack[e].to(DEV),
                                      float(scales[e]), out_dtype=torch.float32))
-        assert np.array_equal(dense, got[offs[z]:offs[z + 1]]), f"group {z} differs from dense"
+        # Both sum exact products in fp32 in their own fixed order (the dense
+        # call may split K): equal within twice the stated tolerance.
+        tol = 2 * oracle.tolerance(bits(rows), oracle.decode_fp8(stack[e].numpy()), float(scales[e]))
+        assert_within(dense, got[offs[z]:offs[z + 1]], tol, f"group {z} vs dense")
 
 
 def test_grouped_max_rows_clips():
