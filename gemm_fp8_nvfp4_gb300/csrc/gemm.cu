@@ -42,6 +42,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "tc.cuh"
 
@@ -196,49 +197,6 @@ template <bool kGrouped>
 __device__ __forceinline__ int num_tiles(const Problem& p) {
   if constexpr (kGrouped) return grouped_num_tiles(p);
   else return plain_num_tiles(p);
-}
-
-// ------------------------------------------------------------- dequant --
-
-// 16 FP8 codes -> 16 bf16 (two 16-byte chunks), exact, NaN preserved.
-__device__ __forceinline__ void fp8x16_to_bf16(uint4 v, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t h01, h23;
-    e4m3x4_to_h2x2(w[i], h01, h23);
-    const float2 a = h2f2(h01);
-    const float2 b = h2f2(h23);
-    o[2 * i] = pack_bf16x2(a.x, a.y);
-    o[2 * i + 1] = pack_bf16x2(b.x, b.y);
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-// 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale ->
-// 16 bf16, exact (the product has at most 6 significant bits).
-__device__ __forceinline__ void nvfp4x16_to_bf16(uint32_t w0, uint32_t w1, float scale, uint4& lo,
-                                                 uint4& hi) {
-  const uint32_t w[2] = {w0, w1};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 e = f16x2_to_f32x2(e2m1x2_to_f16x2(w[i] >> (8 * j)));
-      o[4 * i + j] = pack_bf16x2(e.x * scale, e.y * scale);
-    }
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-// Byte offset of the 16-byte chunk `j` of row `r` in a K-major tile stored
-// with the 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
 // ----------------------------------------------------------------- kernel --
@@ -655,32 +613,6 @@ __global__ void k_fill_scaled_zero(void* out, int bf16_out, int64_t count, float
 
 // --------------------------------------------------------------- host --
 
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle sw) {
-  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-               uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
-  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0, d0 * d1};
-  cuuint32_t box[3] = {b0, b1, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <Fmt F, bool kGrouped>
 cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, const uint8_t* scales,
                    const Problem& p, int grid) {
@@ -755,6 +687,7 @@ int plan_split(const Ctx& c, Problem& p, int tiles) {
 cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* a, const uint8_t* w,
                             int64_t M, int64_t N, int64_t K, float alpha) {
   if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
+  if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, bf16_out, a, w, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -770,6 +703,8 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void
                               const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N, int64_t K,
                               float alpha) {
   if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
+  if (M <= skinny_max_rows())
+    return launch_nvfp4_gemm_skinny(c, out, bf16_out, a, q, bs, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -67,6 +67,15 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out,
                                     int64_t E, int64_t max_rows,
                                     int64_t total_M, int64_t N, int64_t K);
 
+// gemm_skinny.cu (M <= skinny_max_rows())
+int skinny_max_rows();
+cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+                                   const uint8_t* w, int64_t M, int64_t N, int64_t K,
+                                   float alpha);
+cudaError_t launch_nvfp4_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+                                     const uint8_t* q, const uint8_t* bs, int64_t M,
+                                     int64_t N, int64_t K, float alpha);
+
 // api.cu: the driver's cuTensorMapEncodeTiled, resolved once at run time so
 // that the library does not link against libcuda.
 void* tensor_map_encode_fn();

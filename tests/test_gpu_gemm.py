@@ -178,8 +178,8 @@ def test_no_wait_timed_out():
                                    (128, 4096, 1024)])
 def test_small_m_split_k(m, n, k):
     """M <= 128 with few N tiles: K is split over a thread-block cluster and
-    the partials are reduced through distributed shared memory (ragged last
-    split for K = 4112, N not a multiple of the tile)."""
+    the partials are reduced through distributed shared memory (uneven splits
+    for K = 4112, N not a multiple of the tile)."""
     lib()
     check_fp8(m, n, k, seed=m + k)
     if k % 64 == 0:
@@ -193,4 +193,61 @@ def test_small_m_split_k_deterministic():
     w = codes.to(DEV)
     r1 = gq.fp8_matmul(a, w, s, out_dtype=torch.float32)
     r2 = gq.fp8_matmul(a, w, s, out_dtype=torch.float32)
+    assert torch.equal(r1, r2)
+
+
+@pytest.mark.parametrize("m", [1, 2, 15, 16, 17, 31, 48, 64, 65, 100, 127, 128])
+def test_small_m_every_row_count(m):
+    """The few-row kernel (weight as the MMA's A operand, activations as B with
+    N = M rounded up to 16): every padding case of M, N ragged (not a
+    multiple of 4, so the scalar store path runs), bf16 and f32 outputs."""
+    lib()
+    check_fp8(m, 1003, 1024, torch.bfloat16 if m % 2 else torch.float32, seed=m)
+    check_nvfp4(m, 1003, 1024, torch.float32 if m % 2 else torch.bfloat16, seed=m + 7)
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 14336, 4096), (128, 14336, 4096), (5, 4096, 14336)])
+def test_small_m_decode_shapes(m, n, k):
+    """Decode-batch shapes of the FP8 workload: many N tiles (no K split) and a
+    long K with few tiles."""
+    lib()
+    check_fp8(m, n, k, torch.bfloat16, seed=m + n)
+
+
+@pytest.mark.parametrize("m", [1, 40])
+def test_small_m_short_k(m):
+    """K of one or two stages (no split possible) and an FP8 K tail of 16."""
+    lib()
+    check_fp8(m, 384, 16, seed=3)
+    check_fp8(m, 384, 80, seed=4)
+    check_nvfp4(m, 384, 64, seed=5)
+    check_nvfp4(m, 384, 128, seed=6)
+
+
+def test_small_m_identity_dequant_every_fp8_code():
+    """A = I with K = 128: the few-row kernel returns every E4M3 code's value
+    (NaN codes poison their column)."""
+    lib()
+    k = 128
+    codes = (np.arange(300 * k).reshape(300, k) * 11 % 256).astype(np.uint8)
+    eye = torch.eye(k, dtype=torch.bfloat16)
+    c = gq.fp8_matmul(eye.to(DEV), torch.from_numpy(codes).to(DEV), 1.0, out_dtype=torch.float32)
+    want = oracle.fp8_materialize(codes).T.copy()
+    nan_cols = np.isnan(oracle.fp8_materialize(codes)).any(axis=1)
+    want[:, nan_cols] = np.nan
+    assert_exact(to_f64(c), want, "identity fp8 (few rows)", signed_zero=False)
+
+
+def test_small_m_nvfp4_unaligned_scales():
+    """Block scales whose base is 4- but not 16-byte aligned (no L2 prefetch
+    map for them) give the same result as an aligned copy."""
+    lib()
+    q, bs, s2 = synth.nvfp4_weight(512, 4096, seed=21)
+    a = synth.bf16_activations(16, 4096, seed=22).to(DEV)
+    qd = q.to(DEV)
+    store = torch.zeros(bs.numel() + 16, dtype=torch.uint8, device=DEV)
+    shifted = store[4:4 + bs.numel()].view(bs.shape)
+    shifted.copy_(bs.to(DEV))
+    r1 = gq.nvfp4_matmul(a, qd, bs.to(DEV), s2, out_dtype=torch.float32)
+    r2 = gq.nvfp4_matmul(a, qd, shifted, s2, out_dtype=torch.float32)
     assert torch.equal(r1, r2)
