@@ -108,6 +108,34 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return f16x2_to_f32x2(e4m3x2_to_f16x2(code & 0xFFu)).x;
 }
 
+// f16 bits of one float8_e4m3fn code (exact).
+__device__ __forceinline__ uint16_t e4m3_to_f16(uint32_t code) {
+  return static_cast<uint16_t>(e4m3x2_to_f16x2(code & 0xFFu) & 0xFFFFu);
+}
+
+// Both halves of an f16x2 times the f16 s, as two f32: one mixed-precision
+// FMA each (fma.rn.f32.f16, f16 inputs, f32 result).  The addend is -0, which
+// leaves every product and its sign of zero unchanged; the products used here
+// (an E2M1 or E4M3 value times an E4M3 value or 1) have at most 6 significant
+// bits, so they are exact.
+__device__ __forceinline__ float2 h2_scale_f32(uint32_t h2, uint16_t s) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "fma.rn.f32.f16 %0, l, %3, %4;\n\tfma.rn.f32.f16 %1, h, %3, %4;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2), "h"(s), "f"(-0.0f));
+  return make_float2(lo, hi);
+}
+
+// Two floats whose low 16 bits are zero (at most 8 significant bits and in the
+// bf16 range) -> bf16x2 by taking their high halves: no rounding step.  A NaN
+// stays a NaN (the f32 NaNs produced here have a nonzero high mantissa).
+__device__ __forceinline__ uint32_t f32x2_hi_to_bf16x2(float2 v) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r) : "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)));
+  return r;
+}
+
 // Two e4m3 codes in each half of a 32-bit word -> two f16x2 (hardware cvt,
 // exact); the half selection is part of the instruction.
 __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {

@@ -431,8 +431,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint4 v = tc::lds128(w_addr + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
-            const float s0 = e4m3_to_f32(sc >> (16 * c));
-            const float s1 = e4m3_to_f32(sc >> (16 * c + 8));
+            const uint16_t s0 = e4m3_to_f16(sc >> (16 * c));
+            const uint16_t s1 = e4m3_to_f16(sc >> (16 * c + 8));
             uint4 lo, hi;
             nvfp4x16_to_bf16(v.x, v.y, s0, lo, hi);
             tc::sts128(b_addr + sw128_off(row, 4 * c), lo);
@@ -703,7 +703,7 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void
                               const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N, int64_t K,
                               float alpha) {
   if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
-  if (M <= skinny_max_rows())
+  if (M <= skinny_max_rows() && nvfp4_skinny_ok(bs, K))
     return launch_nvfp4_gemm_skinny(c, out, bf16_out, a, q, bs, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,

@@ -15,37 +15,41 @@ namespace gq {
 
 // ------------------------------------------------------------- dequant --
 
+// The decodes below run on the dequant warps' critical path, so they keep the
+// float conversions to one per pair of elements: the hardware cvt to f16x2,
+// then a mixed-precision FMA to f32 (exact), then the bf16 is the f32's high
+// half (exact: every value has at most 6 significant bits).
+
 // 16 FP8 codes -> 16 bf16 (two 16-byte chunks), exact, NaN preserved.
 __device__ __forceinline__ void fp8x16_to_bf16(uint4 v, uint4& lo, uint4& hi) {
+  constexpr uint16_t kOne = 0x3C00;   // 1.0 in f16
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h01, h23;
     e4m3x4_to_h2x2(w[i], h01, h23);
-    const float2 a = h2f2(h01);
-    const float2 b = h2f2(h23);
-    o[2 * i] = pack_bf16x2(a.x, a.y);
-    o[2 * i + 1] = pack_bf16x2(b.x, b.y);
+    o[2 * i] = f32x2_hi_to_bf16x2(h2_scale_f32(h01, kOne));
+    o[2 * i + 1] = f32x2_hi_to_bf16x2(h2_scale_f32(h23, kOne));
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale ->
-// 16 bf16, exact (the product has at most 6 significant bits).
-__device__ __forceinline__ void nvfp4x16_to_bf16(uint32_t w0, uint32_t w1, float scale, uint4& lo,
-                                                 uint4& hi) {
-  const uint32_t w[2] = {w0, w1};
+// 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale
+// (given as f16 bits) -> 16 bf16, exact (the product has at most 6
+// significant bits and lies in [2^-10, 2688]).
+__device__ __forceinline__ void nvfp4x16_to_bf16(uint32_t w0, uint32_t w1, uint16_t scale_h,
+                                                 uint4& lo, uint4& hi) {
   uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 e = f16x2_to_f32x2(e2m1x2_to_f16x2(w[i] >> (8 * j)));
-      o[4 * i + j] = pack_bf16x2(e.x * scale, e.y * scale);
-    }
-  }
+  o[0] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<0>(w0), scale_h));
+  o[1] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<1>(w0), scale_h));
+  o[2] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<2>(w0), scale_h));
+  o[3] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<3>(w0), scale_h));
+  o[4] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<0>(w1), scale_h));
+  o[5] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<1>(w1), scale_h));
+  o[6] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<2>(w1), scale_h));
+  o[7] = f32x2_hi_to_bf16x2(h2_scale_f32(e2m1x2_b<3>(w1), scale_h));
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }

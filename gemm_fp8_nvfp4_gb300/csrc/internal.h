@@ -69,6 +69,7 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out,
 
 // gemm_skinny.cu (M <= skinny_max_rows())
 int skinny_max_rows();
+bool nvfp4_skinny_ok(const uint8_t* bs, int64_t K);   // the NVFP4 few-row kernel takes this K
 cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
                                    const uint8_t* w, int64_t M, int64_t N, int64_t K,
                                    float alpha);

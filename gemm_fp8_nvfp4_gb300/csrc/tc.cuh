@@ -253,6 +253,12 @@ __device__ __forceinline__ void cluster_sync() {
                    "memory");
 }
 
+// Barrier over every thread of every CTA of the cluster, without memory
+// ordering (for when only execution order matters).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Shared-memory address of this CTA -> the same offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, int rank) {
   uint32_t r;
