@@ -248,6 +248,10 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + (v + u * kThreads) * VEC, wv[u][r]);
+      if (!waited) {
+        pdl_wait_ordered();
+        waited = true;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float xf[VEC];
@@ -260,6 +264,10 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       uint32_t wv[R][kWords];
 #pragma unroll
       for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + v * VEC, wv[r]);
+      if (!waited) {
+        pdl_wait_ordered();
+        waited = true;
+      }
       float xf[VEC];
       load_x<VEC>(x, v * VEC, xf);
 #pragma unroll
@@ -423,21 +431,9 @@ cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* 
                               const uint8_t* q, const uint8_t* bs, int64_t N,
                               int64_t K, float alpha) {
   const uint16_t* xb = static_cast<const uint16_t*>(x);
-  const bool wide = (K % 32 == 0) && (reinterpret_cast<uintptr_t>(bs) % 2 == 0);
-  if (wide) {
-    // 8 rows per CTA, one 16-byte vector per row per step (best at N = K = 4096).
-    constexpr int kRowsWide = 8;
-    const int64_t grid = (N + kRowsWide - 1) / kRowsWide;
-    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    if (c.overlap_weights) {
-      return launch_kernel(c, true, k_nvfp4_gemv<16, kRowsWide, 1, kThreads, true>,
-                           dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb,
-                           q, bs, N, K, alpha);
-    }
-    return launch_kernel(c, false, k_nvfp4_gemv<16, kRowsWide, 1>,
-                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
-                         bs, N, K, alpha);
-  }
+  // 4 rows per CTA, two 8-byte vectors (one 16-element block each) per row
+  // per step: measured best at N = K = 4096 against 16-byte vectors and
+  // other row / vector / CTA-size splits.
   const int64_t grid = (N + kRows - 1) / kRows;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {

@@ -193,11 +193,12 @@ def test_overlap_flag_gives_identical_results(overlap_flag):
     assert torch.equal(on8, off8) and torch.equal(on4, off4)
 
 
-def test_overlap_flag_orders_activation_reads(overlap_flag):
+@pytest.mark.parametrize("n", [4096, 4104, 4098])
+def test_overlap_flag_orders_activation_reads(overlap_flag, n):
     """A chain of dependent GEMVs (the output of one is the input of the next)
     and a torch kernel writing x right before a GEMV: with the overlap flag
-    every x read still sees the previous kernel's result."""
-    n = 4096
+    every x read still sees the previous kernel's result.  n = 4104 and 4098
+    take the 8- and 2-byte weight-vector paths."""
     codes = [synth.fp8_weight(n, n, seed=30 + i)[0] for i in range(3)]
     ws = [c.to(DEV) for c in codes]
     x0 = synth.bf16_activations(1, n, seed=40).reshape(-1)
