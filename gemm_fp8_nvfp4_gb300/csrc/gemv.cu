@@ -248,10 +248,6 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + (v + u * kThreads) * VEC, wv[u][r]);
-      if (!waited) {
-        pdl_wait_ordered();
-        waited = true;
-      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float xf[VEC];
@@ -264,10 +260,6 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
       uint32_t wv[R][kWords];
 #pragma unroll
       for (int r = 0; r < R; ++r) load_w8<VEC>(rows[r] + v * VEC, wv[r]);
-      if (!waited) {
-        pdl_wait_ordered();
-        waited = true;
-      }
       float xf[VEC];
       load_x<VEC>(x, v * VEC, xf);
 #pragma unroll
