@@ -20,12 +20,16 @@
 // Weight loads bypass L1 (read once); activation loads go through L1 because
 // every CTA on the SM reads the same x.
 //
-// With GQ_LAUNCH_OVERLAP_WEIGHT_READS the GEMV is launched as a programmatic
-// dependent of the previous kernel in the stream: each thread issues its first
-// batch of weight loads, then waits (griddepcontrol.wait) for that kernel to
-// complete before it reads x or writes y.  The weight stream of one GEMV thus overlaps the tail
-// of the previous kernel -- valid only when that kernel does not write the
-// weights, which is why it is opt-in.
+// Every GEMV is launched as a programmatic dependent of the previous kernel
+// in the stream (the programmatic stream serialization attribute) and calls
+// griddepcontrol.launch_dependents at its start: its CTAs become resident
+// while the previous kernel finishes and wait (griddepcontrol.wait) before
+// touching global memory, so stream order is kept and the launch gap between
+// back-to-back GEMVs is hidden.  With GQ_LAUNCH_OVERLAP_WEIGHT_READS each
+// thread issues its first batch of weight loads before that wait, and reads
+// x and writes y only after it: the weight stream of one GEMV overlaps the
+// tail of the previous kernel -- valid only when that kernel does not write
+// the weights, which is why it is opt-in.
 //
 // The load width adapts to K and the pointers: 16 bytes when K % 16 == 0,
 // down to 1 byte for odd K (the pages' scalar tail for K % TILE_K != 0 becomes
@@ -174,8 +178,13 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
   const int64_t nvec = K / VEC;
   // Overlap mode: the first batch of weight loads is issued before the wait
   // for the previous kernel; x is read and y written only after it.
-  if constexpr (kOverlap) pdl_launch_dependents();
-  if constexpr (kOverlap && VEC != 16) pdl_wait_ordered();
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: the CTAs become resident while that kernel finishes.  Plain
+  // order waits for it before touching any global memory; overlap mode
+  // waits after its first batch of weight loads.  Every GEMV lets the next
+  // kernel's CTAs launch early too.
+  pdl_launch_dependents();
+  if constexpr (!kOverlap || VEC != 16) pdl_wait();
   bool waited = !kOverlap || VEC != 16;
   constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
 
@@ -315,7 +324,9 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
   __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t half_k = K / 2;
-  if constexpr (kOverlap) pdl_launch_dependents();
+  // Programmatic dependent launch as in k_fp8_gemv.
+  pdl_launch_dependents();
+  if constexpr (!kOverlap) pdl_wait();
   bool waited = !kOverlap;
   const int64_t nvec = half_k / VB;
   constexpr int kWords = VB / 4;
@@ -398,7 +409,7 @@ cudaError_t fp8_dispatch(const Ctx& c, void* y, bool bf16_out, const void* x,
                          dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
                          static_cast<const uint16_t*>(x), w, N, K, alpha);
   }
-  return launch_kernel(c, false, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)>,
+  return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)>,
                        dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
                        static_cast<const uint16_t*>(x), w, N, K, alpha);
 }
@@ -433,7 +444,7 @@ cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* 
                          dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
                          bs, N, K, alpha);
   }
-  return launch_kernel(c, false, k_nvfp4_gemv<8, kRows, 2>,
+  return launch_kernel(c, true, k_nvfp4_gemv<8, kRows, 2>,
                        dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
                        bs, N, K, alpha);
 }
