@@ -14,12 +14,16 @@ with numpy:
 * the linear layer (``linear``): a float64 dot product of the bf16 activations
   with the decoded weight, times the per-tensor scale folded after the sum;
   the grouped (MoE) form loops over groups and runs a dense product per group;
-  materialize returns the decoded weight itself.
+  materialize returns the decoded weight itself;
+* the optional fused epilogue (``epilogue``): bias add and an activation,
+  and the binary16 output rounding (``formats.f64_to_f16_bits``).
 
 Sources (Modular kernel API pages for Apple M5):
   * "fp8_gemv" module page: the W8A16 GEMV, the scale contract, materialize;
   * "fp4_matmul" module page: the packed NVFP4 weight layout and block scales;
-  * "Matmul2dFp8" struct page, method ``run_grouped``: the grouped MoE product.
+  * "Matmul2dFp8" struct page, method ``run_grouped``: the grouped MoE product;
+    its parameters c_type (fp16 / bf16 / fp32 output) and elementwise_lambda_fn
+    (the fused epilogue).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against what the
 pages and the formats fix (exhaustive code tables, closed forms, brute force in
@@ -27,7 +31,8 @@ exact rational arithmetic, invariants).  The pages print no worked numerical
 example of the layer itself, so no function is pinned to a printed value.
 """
 
-from .formats import e4m3_table, e2m1_table, bf16_bits_to_f64, f64_to_bf16_bits
+from .formats import (e4m3_table, e2m1_table, bf16_bits_to_f64, f64_to_bf16_bits,
+                      f16_bits_to_f64, f64_to_f16_bits)
 from .decode import decode_fp8, decode_nvfp4, nibble
 from .layer import (
     linear,
@@ -42,6 +47,11 @@ from .layer import (
     abs_dot,
     bf16_ulp,
     tolerance,
+    f16_ulp,
+    activation,
+    ACT_LIPSCHITZ,
+    epilogue,
+    tolerance_epilogue,
 )
 
 __all__ = [
@@ -50,4 +60,6 @@ __all__ = [
     "linear", "linear_loops", "fp8_gemv", "fp8_matmul", "nvfp4_gemv",
     "nvfp4_matmul", "fp8_grouped_matmul", "fp8_materialize",
     "nvfp4_materialize", "abs_dot", "bf16_ulp", "tolerance",
+    "f16_bits_to_f64", "f64_to_f16_bits", "f16_ulp", "activation", "ACT_LIPSCHITZ",
+    "epilogue", "tolerance_epilogue",
 ]

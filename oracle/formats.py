@@ -14,6 +14,9 @@ Test infrastructure only (see the package docstring).
   (bit 3), two exponent bits (bias 1), one mantissa bit; exponent field 0 is
   the subnormal m * 0.5.  Magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
 * bfloat16 -- the activation type: the top 16 bits of an IEEE binary32.
+* binary16 (fp16) -- an output type (the "Matmul2dFp8" struct page lists fp16,
+  bf16 and fp32 for c_type): one sign bit, five exponent bits (bias 15), ten
+  mantissa bits; exponent field 0 encodes the subnormals m/1024 * 2^-14.
 """
 
 import math
@@ -113,3 +116,60 @@ def _one_f64_to_bf16(x: float) -> int:
     exp_field = (e3 - 1) + 127
     mant = int(math.ldexp(m2, 8)) - 128       # 7 stored bits
     return sign | (exp_field << 7) | mant
+
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns (uint16) -> float64, decoded from the fields."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    m = (b & 0x3FF).astype(np.float64)
+    normal = sign * (1.0 + m / 1024.0) * np.ldexp(1.0, (e - 15))
+    sub = sign * (m / 1024.0) * 2.0 ** -14
+    special = np.where(m == 0, sign * np.inf, np.nan)
+    return np.where(e == 0x1F, special, np.where(e == 0, sub, normal))
+
+
+def f64_to_f16_bits(v) -> np.ndarray:
+    """float64 -> binary16 bit patterns with round-to-nearest-even.
+
+    Same construction as the bfloat16 rounding: the value's quantum is
+    2^(e-10) for magnitudes in [2^e, 2^(e+1)) and 2^-24 below 2^-14 (the
+    subnormals); round to a multiple of it, ties to the even multiple; a
+    rounded magnitude of 2^16 or more is infinity (largest finite 65504).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    flat_in = v.reshape(-1)
+    flat_out = out.reshape(-1)
+    for i, x in enumerate(flat_in):
+        flat_out[i] = _one_f64_to_f16(float(x))
+    return out
+
+
+def _one_f64_to_f16(x: float) -> int:
+    sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
+    if math.isnan(x):
+        return sign | 0x7E00
+    a = abs(x)
+    if math.isinf(a):
+        return sign | 0x7C00
+    if a == 0.0:
+        return sign
+    m, e = math.frexp(a)
+    e2 = e - 1
+    q_exp = max(e2, -14) - 10
+    scaled = math.ldexp(a, -q_exp)
+    n = math.floor(scaled)
+    frac = scaled - n
+    if frac > 0.5 or (frac == 0.5 and (n & 1)):
+        n += 1
+    r = math.ldexp(n, q_exp)
+    if r >= 2.0 ** 16:
+        return sign | 0x7C00
+    if r < 2.0 ** -14:
+        return sign | int(math.ldexp(r, 24))          # subnormal: r = mant * 2^-24
+    m2, e3 = math.frexp(r)
+    exp_field = (e3 - 1) + 15
+    mant = int(math.ldexp(m2, 11)) - 1024             # 10 stored bits
+    return sign | (exp_field << 10) | mant

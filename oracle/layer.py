@@ -31,7 +31,7 @@ import math
 import numpy as np
 
 from .decode import decode_fp8, decode_nvfp4
-from .formats import bf16_bits_to_f64
+from .formats import bf16_bits_to_f64, f16_bits_to_f64
 
 
 def _activations(x) -> np.ndarray:
@@ -172,4 +172,80 @@ def tolerance(x, w_hat, alpha=1.0, out_bf16=False, ref=None) -> np.ndarray:
         if ref is None:
             ref = linear(x, w_hat, alpha)
         tol = tol + bf16_ulp(np.abs(ref) + tol)
+    return tol
+
+
+# ------------------------------------------------------------------ epilogue --
+#
+# The "Matmul2dFp8" struct page gives the tiled matmul an optional fused
+# epilogue: an elementwise function of the output coordinate (row, col) and
+# the computed value, applied where the result is stored.  The layer's
+# epilogue, in the order a linear layer applies it, is
+#
+#     out[m, n] = act(alpha * sum_k x[m, k] w_hat[n, k] + bias[n])
+#
+# (grouped: the bias row of the group's expert), with act one of the
+# activations below, written from their definitions.
+
+def f16_ulp(v) -> np.ndarray:
+    """Spacing of binary16 numbers at |v| (2^(e-10) for |v| in [2^e, 2^(e+1)),
+    2^-24 below the smallest normal 2^-14)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, e = np.frexp(np.where(np.isfinite(a), a, 0.0))
+    ulp = np.ldexp(1.0, (e - 1 - 10).astype(np.int64))
+    return np.where((a < 2.0 ** -14) | ~np.isfinite(a), 2.0 ** -24, ulp)
+
+
+def activation(v, kind: str) -> np.ndarray:
+    """Elementwise activation, float64.
+
+    none:      v
+    relu:      v for v > 0, else 0 (NaN stays NaN)
+    silu:      v / (1 + exp(-v))                      (v times the logistic sigmoid)
+    gelu_tanh: 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))   (tanh form of GELU)
+    """
+    v = np.asarray(v, dtype=np.float64)
+    if kind == "none":
+        return v.copy()
+    if kind == "relu":
+        return np.where(v > 0, v, np.where(np.isnan(v), v, 0.0))
+    if kind == "silu":
+        with np.errstate(over="ignore", invalid="ignore"):
+            return v / (1.0 + np.exp(-v))
+    if kind == "gelu_tanh":
+        c = math.sqrt(2.0 / math.pi)
+        with np.errstate(over="ignore", invalid="ignore"):
+            return 0.5 * v * (1.0 + np.tanh(c * (v + 0.044715 * v ** 3)))
+    raise ValueError(f"unknown activation {kind!r}")
+
+
+# Upper bounds of |d act / dv| over the reals: how far an error in the
+# pre-activation value can move the output.
+ACT_LIPSCHITZ = {"none": 1.0, "relu": 1.0, "silu": 1.1, "gelu_tanh": 1.13}
+
+
+def epilogue(v, bias=None, act: str = "none") -> np.ndarray:
+    """act(v + bias) with bias broadcast along the last axis (the column n)."""
+    v = np.asarray(v, dtype=np.float64)
+    if bias is not None:
+        v = v + np.asarray(bias, dtype=np.float64)
+    return activation(v, act)
+
+
+def tolerance_epilogue(tol_pre, ref_out, act: str = "none", out_kind: str = "f32") -> np.ndarray:
+    """Allowed |gpu - oracle| after the epilogue.
+
+    tol_pre is the allowed error of the pre-activation value (``tolerance``
+    without the output rounding).  The activation moves it by at most its
+    Lipschitz bound; the fp32 bias add and the fp32 activation functions add
+    a few units in the last place of the fp32 result (2^-20 |out| covers
+    them); the output conversion adds one unit in the last place of the
+    output type.
+    """
+    ref = np.abs(np.asarray(ref_out, dtype=np.float64))
+    tol = ACT_LIPSCHITZ[act] * np.asarray(tol_pre, dtype=np.float64) + 2.0 ** -20 * ref
+    if out_kind == "bf16":
+        tol = tol + bf16_ulp(ref + tol)
+    elif out_kind == "f16":
+        tol = tol + f16_ulp(ref + tol)
     return tol

@@ -395,10 +395,84 @@ def check_tolerance_shape(orc):
     assert tb[0, 0] == 2e-4 * 11.0 + 2.0 ** -5
 
 
+def check_f16_decode(orc):
+    """Every binary16 pattern decodes to numpy's float16 value (a library
+    special case of the same format), NaN exactly at the NaN patterns."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.f16_bits_to_f64(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    m = ~np.isnan(want)
+    assert np.array_equal(got[m], want[m])
+    assert np.array_equal(np.signbit(got[m]), np.signbit(want[m]))
+    assert got[0x7BFF] == 65504.0 and got[0x0001] == 2.0 ** -24 and got[0x7C00] == np.inf
+
+
+def check_f16_rounding(orc, seed=21):
+    """float64 -> binary16 RNE agrees with numpy's conversion on values at
+    every scale, on exact ties between neighbours (both parities), around
+    the overflow threshold and in the subnormal range."""
+    rng = np.random.default_rng(seed)
+    vals = [rng.standard_normal(400) * 10.0 ** rng.integers(-9, 6, 400)]
+    halves = orc.f16_bits_to_f64(np.arange(0, 0x7C00, 97, dtype=np.uint32).astype(np.uint16))
+    nxt = orc.f16_bits_to_f64(np.arange(1, 0x7C01, 97, dtype=np.uint32).astype(np.uint16))
+    vals.append((halves + nxt) / 2.0)                      # exact midpoints (ties)
+    vals.append(np.array([65504.0, 65519.999, 65520.0, 65536.0, 1e6, 2.0 ** -25, 3 * 2.0 ** -26,
+                          2.0 ** -24 * 1.5, -0.0, 0.0, np.inf, -np.inf]))
+    v = np.concatenate(vals)
+    v = np.concatenate([v, -v])
+    got = orc.f64_to_f16_bits(v)
+    with np.errstate(over="ignore"):
+        want = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+    assert orc.f64_to_f16_bits(np.array([np.nan]))[0] & 0x7C00 == 0x7C00
+
+
+def check_activations(orc):
+    """Activations against what their definitions fix: ReLU's closed form;
+    the odd parts of SiLU and tanh-GELU are v / 2 (act(v) - act(-v) = v);
+    slope 1/2 at 0; SiLU's sigmoid limits; tanh-GELU within the approximation's
+    known distance (< 1e-3) of the erf form 0.5 v (1 + erf(v / sqrt 2));
+    the Lipschitz bounds the tolerance uses are tight upper bounds."""
+    v = np.linspace(-8.0, 8.0, 3201)
+    r = orc.activation(v, "relu")
+    assert np.array_equal(r, np.where(v > 0, v, 0.0))
+    assert np.isnan(orc.activation(np.array([np.nan]), "relu")[0])
+    assert np.array_equal(orc.activation(v, "none"), v)
+    for kind in ("silu", "gelu_tanh"):
+        a = orc.activation(v, kind)
+        assert np.allclose(a - orc.activation(-v, kind), v, rtol=1e-12, atol=1e-12)
+        h = 1e-6
+        d0 = (orc.activation(np.array([h]), kind) - orc.activation(np.array([-h]), kind))[0] / (2 * h)
+        assert abs(d0 - 0.5) < 1e-6
+        slope = np.max(np.abs(np.diff(a) / np.diff(v)))
+        assert orc.ACT_LIPSCHITZ[kind] - 0.02 < slope <= orc.ACT_LIPSCHITZ[kind]
+    s = orc.activation(np.array([40.0, -40.0, 0.0]), "silu")
+    assert abs(s[0] - 40.0) < 1e-12 and abs(s[1]) < 1e-15 and s[2] == 0.0
+    g = orc.activation(v, "gelu_tanh")
+    erf_form = np.array([0.5 * t * (1.0 + math.erf(t / math.sqrt(2.0))) for t in v])
+    assert np.max(np.abs(g - erf_form)) < 1e-3
+
+
+def check_epilogue(orc):
+    """The bias is added per output column before the activation."""
+    v = np.array([[1.0, -1.0], [0.5, 4.0]])
+    b = np.array([-2.0, 3.0])
+    out = orc.epilogue(v, b, "relu")
+    assert np.array_equal(out, np.array([[0.0, 2.0], [0.0, 7.0]]))
+    assert np.array_equal(orc.epilogue(v, None, "none"), v)
+    # tolerance: Lipschitz bound x pre-activation tolerance + 2^-20 |out| (+ output ulp)
+    t = orc.tolerance_epilogue(np.array([1e-3]), np.array([3.0]), "silu", "f32")
+    assert t[0] == 1.1 * 1e-3 + 3.0 * 2.0 ** -20
+    t16 = orc.tolerance_epilogue(np.array([0.0]), np.array([3.0]), "none", "f16")
+    assert t16[0] == 3.0 * 2.0 ** -20 + 2.0 ** -9      # f16 ulp on [2, 4) is 2^-9
+
+
 ALL_CHECKS = [
     check_e4m3_table, check_e2m1_table, check_bf16_exactness, check_bf16_rounding,
     check_bf16_decode, check_fp8_worked, check_nvfp4_worked, check_grouped_worked,
     check_bruteforce_fp8, check_bruteforce_nvfp4, check_nvfp4_materialize_independent,
     check_fp8_materialize_independent, check_scale_fold, check_gemv_is_gemm_row,
-    check_grouped_vs_dense, check_tolerance_shape,
+    check_grouped_vs_dense, check_tolerance_shape, check_f16_decode, check_f16_rounding,
+    check_activations, check_epilogue,
 ]

@@ -91,6 +91,42 @@ def _linear_drop_last_k(x, w_hat, alpha=1.0):
     return float(alpha) * (xf[..., :-1] @ w[:, :-1].T)
 
 
+def _f16_ties_away(x: float) -> int:
+    # round half away from zero instead of to even
+    import math
+    sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
+    a = abs(x)
+    if math.isnan(a) or math.isinf(a) or a == 0.0:
+        return ORIG_F16(x)
+    m, e = math.frexp(a)
+    q_exp = max(e - 1, -14) - 10
+    n = math.floor(math.ldexp(a, -q_exp) + 0.5)
+    return ORIG_F16(math.copysign(math.ldexp(n, q_exp), -1.0 if sign else 1.0))
+
+
+def _gelu_wrong_constant(v, kind):
+    if kind == "gelu_tanh":
+        v = np.asarray(v, dtype=np.float64)
+        c = (2.0 / np.pi) ** 0.5
+        return 0.5 * v * (1.0 + np.tanh(c * (v + 0.0447 * v ** 2)))
+    return ORIG_ACT(v, kind)
+
+
+def _silu_wrong_sign(v, kind):
+    if kind == "silu":
+        v = np.asarray(v, dtype=np.float64)
+        with np.errstate(over="ignore"):
+            return v / (1.0 + np.exp(v))
+    return ORIG_ACT(v, kind)
+
+
+def _epilogue_act_first(v, bias=None, act="none"):
+    out = oracle.layer.activation(v, act)
+    return out if bias is None else out + np.asarray(bias, dtype=np.float64)
+
+
+ORIG_F16 = oracle.formats._one_f64_to_f16
+ORIG_ACT = oracle.layer.activation
 ORIG_DECODE_NVFP4 = oracle.decode.decode_nvfp4
 ORIG_LINEAR = oracle.layer.linear
 
@@ -107,6 +143,13 @@ MUTATIONS = {
     "scale_not_folded": [(oracle.layer, "linear", _linear_drop_alpha)],
     "abs_of_weights": [(oracle.layer, "linear", _linear_abs_weights)],
     "dropped_last_term": [(oracle.layer, "linear", _linear_drop_last_k)],
+    "f16_ties_away": [(oracle.formats, "_one_f64_to_f16", _f16_ties_away)],
+    "gelu_wrong_cubic": [(oracle.layer, "activation", _gelu_wrong_constant),
+                         (oracle, "activation", _gelu_wrong_constant)],
+    "silu_wrong_sign": [(oracle.layer, "activation", _silu_wrong_sign),
+                        (oracle, "activation", _silu_wrong_sign)],
+    "activation_before_bias": [(oracle.layer, "epilogue", _epilogue_act_first),
+                               (oracle, "epilogue", _epilogue_act_first)],
 }
 
 
