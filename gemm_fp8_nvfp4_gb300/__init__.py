@@ -11,8 +11,10 @@ the calls raise.
 
 Entry points (same names as the C ABI without the ``gq_`` prefix):
 ``fp8_gemv``, ``nvfp4_gemv``, ``fp8_matmul``, ``nvfp4_matmul``,
-``fp8_grouped_matmul``, ``fp8_materialize``, ``nvfp4_materialize``.
-Host-buffer variants for end-to-end timing live in ``host``.
+``fp8_grouped_matmul``, ``fp8_materialize``, ``nvfp4_materialize``.  The
+product calls take ``bias=`` and ``activation=`` for the fused epilogue
+(``out = act(alpha * acc + bias)``); with either given they call the ``_ex``
+form of the C entry point.  Outputs may be float32, bfloat16 or float16.
 """
 
 from __future__ import annotations
@@ -25,10 +27,19 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgq.so")
 
-GQ_F32, GQ_BF16 = 0, 1
+GQ_F32, GQ_BF16, GQ_F16 = 0, 1, 2
+
+ACTIVATIONS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+
+
+class Epilogue(ctypes.Structure):
+    """struct gq_epilogue."""
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int),
+                ("activation", ctypes.c_int)]
 
 # Names and argument types of every exported symbol (mirrors include/gq.h).
 _P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+_E = ctypes.POINTER(Epilogue)
 SIGNATURES = {
     "gq_status_str": (ctypes.c_char_p, [_I]),
     "gq_version": (ctypes.c_char_p, []),
@@ -38,6 +49,12 @@ SIGNATURES = {
     "gq_nvfp4_matmul": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _F, _P]),
     "gq_fp8_grouped_matmul": (_I, [_P, _I, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                    _I64, _I64, _P]),
+    "gq_fp8_gemv_ex": (_I, [_P, _I, _P, _P, _I64, _I64, _F, _E, _P]),
+    "gq_nvfp4_gemv_ex": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _F, _E, _P]),
+    "gq_fp8_matmul_ex": (_I, [_P, _I, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
+    "gq_nvfp4_matmul_ex": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
+    "gq_fp8_grouped_matmul_ex": (_I, [_P, _I, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                      _I64, _I64, _E, _P]),
     "gq_fp8_materialize": (_I, [_P, _I, _P, _I64, _I64, _P]),
     "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
@@ -115,7 +132,28 @@ def _out_code(dtype) -> int:
         return GQ_F32
     if dtype == torch.bfloat16:
         return GQ_BF16
-    raise TypeError("output dtype must be torch.float32 or torch.bfloat16")
+    if dtype == torch.float16:
+        return GQ_F16
+    raise TypeError("dtype must be torch.float32, torch.bfloat16 or torch.float16")
+
+
+def _epilogue(bias, activation, shape):
+    """A gq_epilogue for bias / activation, or None when neither is given."""
+    if bias is None and activation in (None, "none"):
+        return None
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    ep = Epilogue(None, GQ_F32, ACTIVATIONS[activation])
+    if bias is not None:
+        if tuple(bias.shape) != tuple(shape):
+            raise ValueError(f"bias must have shape {tuple(shape)}")
+        ep.bias = _dev(bias, "bias")
+        ep.bias_dtype = _out_code(bias.dtype)
+    return ep
+
+
+def _ref(ep):
+    return ctypes.byref(ep)
 
 
 def _out(out, shape, dtype, device):
@@ -132,8 +170,9 @@ def _u8(t, name, ndim):
     return t, _dev(t, name, torch.uint8, ndim)
 
 
-def fp8_gemv(x, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
-    """y[N] = alpha * x[K] @ e4m3(w[N, K])^T."""
+def fp8_gemv(x, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None, bias=None,
+             activation="none"):
+    """y[N] = act(alpha * x[K] @ e4m3(w[N, K])^T + bias)."""
     w, wp = _u8(w, "w", 2)
     n, k = w.shape
     xp = _dev(x.reshape(-1), "x", torch.bfloat16, 1)
@@ -141,13 +180,21 @@ def fp8_gemv(x, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
         raise ValueError("x must have K elements")
     dtype = out.dtype if out is not None else out_dtype
     y = _out(out, (n,), dtype, w.device)
-    _check(load_library().gq_fp8_gemv(_dev(y, "out"), _out_code(dtype), xp, wp, n, k,
-                                      float(alpha), _stream_handle(stream)), "fp8_gemv")
+    ep = _epilogue(bias, activation, (n,))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_fp8_gemv(_dev(y, "out"), _out_code(dtype), xp, wp, n, k, float(alpha),
+                             _stream_handle(stream))
+    else:
+        st = lib.gq_fp8_gemv_ex(_dev(y, "out"), _out_code(dtype), xp, wp, n, k, float(alpha),
+                                _ref(ep), _stream_handle(stream))
+    _check(st, "fp8_gemv")
     return y
 
 
-def nvfp4_gemv(x, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
-    """y[N] = alpha * x[K] @ (e2m1(q) * e4m3(bs))^T;  q [N, K/2], bs [N, K/16]."""
+def nvfp4_gemv(x, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None, bias=None,
+               activation="none"):
+    """y[N] = act(alpha * x[K] @ (e2m1(q) * e4m3(bs))^T + bias);  q [N, K/2], bs [N, K/16]."""
     q, qp = _u8(q, "q", 2)
     bs, bp = _u8(bs, "bs", 2)
     n, half = q.shape
@@ -157,13 +204,21 @@ def nvfp4_gemv(x, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=N
         raise ValueError("shapes must be x [K], q [N, K/2], bs [N, K/16]")
     dtype = out.dtype if out is not None else out_dtype
     y = _out(out, (n,), dtype, q.device)
-    _check(load_library().gq_nvfp4_gemv(_dev(y, "out"), _out_code(dtype), xp, qp, bp, n, k,
-                                        float(alpha), _stream_handle(stream)), "nvfp4_gemv")
+    ep = _epilogue(bias, activation, (n,))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_nvfp4_gemv(_dev(y, "out"), _out_code(dtype), xp, qp, bp, n, k, float(alpha),
+                               _stream_handle(stream))
+    else:
+        st = lib.gq_nvfp4_gemv_ex(_dev(y, "out"), _out_code(dtype), xp, qp, bp, n, k,
+                                  float(alpha), _ref(ep), _stream_handle(stream))
+    _check(st, "nvfp4_gemv")
     return y
 
 
-def fp8_matmul(a, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
-    """c[M, N] = alpha * a[M, K] @ e4m3(w[N, K])^T."""
+def fp8_matmul(a, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None, bias=None,
+               activation="none"):
+    """c[M, N] = act(alpha * a[M, K] @ e4m3(w[N, K])^T + bias[N])."""
     w, wp = _u8(w, "w", 2)
     ap = _dev(a, "a", torch.bfloat16, 2)
     m, k = a.shape
@@ -172,13 +227,21 @@ def fp8_matmul(a, w, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None)
         raise ValueError("a and w disagree on K")
     dtype = out.dtype if out is not None else out_dtype
     c = _out(out, (m, n), dtype, a.device)
-    _check(load_library().gq_fp8_matmul(_dev(c, "out"), _out_code(dtype), ap, wp, m, n, k,
-                                        float(alpha), _stream_handle(stream)), "fp8_matmul")
+    ep = _epilogue(bias, activation, (n,))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_fp8_matmul(_dev(c, "out"), _out_code(dtype), ap, wp, m, n, k, float(alpha),
+                               _stream_handle(stream))
+    else:
+        st = lib.gq_fp8_matmul_ex(_dev(c, "out"), _out_code(dtype), ap, wp, m, n, k, float(alpha),
+                                  _ref(ep), _stream_handle(stream))
+    _check(st, "fp8_matmul")
     return c
 
 
-def nvfp4_matmul(a, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None):
-    """c[M, N] = alpha * a[M, K] @ (e2m1(q) * e4m3(bs))^T."""
+def nvfp4_matmul(a, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream=None, bias=None,
+                 activation="none"):
+    """c[M, N] = act(alpha * a[M, K] @ (e2m1(q) * e4m3(bs))^T + bias[N])."""
     q, qp = _u8(q, "q", 2)
     bs, bp = _u8(bs, "bs", 2)
     ap = _dev(a, "a", torch.bfloat16, 2)
@@ -188,17 +251,26 @@ def nvfp4_matmul(a, q, bs, alpha=1.0, out=None, out_dtype=torch.bfloat16, stream
         raise ValueError("shapes must be a [M, K], q [N, K/2], bs [N, K/16]")
     dtype = out.dtype if out is not None else out_dtype
     c = _out(out, (m, n), dtype, a.device)
-    _check(load_library().gq_nvfp4_matmul(_dev(c, "out"), _out_code(dtype), ap, qp, bp, m, n, k,
-                                          float(alpha), _stream_handle(stream)), "nvfp4_matmul")
+    ep = _epilogue(bias, activation, (n,))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_nvfp4_matmul(_dev(c, "out"), _out_code(dtype), ap, qp, bp, m, n, k,
+                                 float(alpha), _stream_handle(stream))
+    else:
+        st = lib.gq_nvfp4_matmul_ex(_dev(c, "out"), _out_code(dtype), ap, qp, bp, m, n, k,
+                                    float(alpha), _ref(ep), _stream_handle(stream))
+    _check(st, "nvfp4_matmul")
     return c
 
 
 def fp8_grouped_matmul(a, w, a_offsets, expert_ids, expert_scales=None, max_rows_per_group=None,
-                       out=None, out_dtype=torch.bfloat16, stream=None):
+                       out=None, out_dtype=torch.bfloat16, stream=None, bias=None,
+                       activation="none"):
     """Grouped MoE product.  a [total_M, K] bf16, w [E, N, K] e4m3,
     a_offsets [G+1] uint32/int32 (device), expert_ids [G] int32 (device),
-    expert_scales [E] float32 or None.  Rows no group covers are left as they
-    are in `out` (allocate it yourself to control them)."""
+    expert_scales [E] float32 or None, bias [E, N] or None (fused epilogue
+    per expert).  Rows no group covers are left as they are in `out`
+    (allocate it yourself to control them)."""
     w, wp = _u8(w, "w", 3)
     ap = _dev(a, "a", torch.bfloat16, 2)
     total_m, k = a.shape
@@ -217,14 +289,22 @@ def fp8_grouped_matmul(a, w, a_offsets, expert_ids, expert_scales=None, max_rows
         max_rows_per_group = total_m
     dtype = out.dtype if out is not None else out_dtype
     c = _out(out, (total_m, n), dtype, a.device)
-    _check(load_library().gq_fp8_grouped_matmul(
-        _dev(c, "out"), _out_code(dtype), ap, wp, op, ip, sp, g, e, int(max_rows_per_group),
-        total_m, n, k, _stream_handle(stream)), "fp8_grouped_matmul")
+    ep = _epilogue(bias, activation, (e, n))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_fp8_grouped_matmul(_dev(c, "out"), _out_code(dtype), ap, wp, op, ip, sp, g, e,
+                                       int(max_rows_per_group), total_m, n, k,
+                                       _stream_handle(stream))
+    else:
+        st = lib.gq_fp8_grouped_matmul_ex(_dev(c, "out"), _out_code(dtype), ap, wp, op, ip, sp, g,
+                                          e, int(max_rows_per_group), total_m, n, k, _ref(ep),
+                                          _stream_handle(stream))
+    _check(st, "fp8_grouped_matmul")
     return c
 
 
 def fp8_materialize(w, out=None, out_dtype=torch.bfloat16, stream=None):
-    """Dense e4m3(w) [N, K] as float32 or bf16 (exact, unscaled)."""
+    """Dense e4m3(w) [N, K] as float32, bf16 or float16 (exact, unscaled)."""
     w, wp = _u8(w, "w", 2)
     n, k = w.shape
     dtype = out.dtype if out is not None else out_dtype
@@ -235,7 +315,7 @@ def fp8_materialize(w, out=None, out_dtype=torch.bfloat16, stream=None):
 
 
 def nvfp4_materialize(q, bs, out=None, out_dtype=torch.bfloat16, stream=None):
-    """Dense e2m1(q) * e4m3(bs) [N, K] as float32 or bf16 (exact, unscaled)."""
+    """Dense e2m1(q) * e4m3(bs) [N, K] as float32, bf16 or float16 (exact, unscaled)."""
     q, qp = _u8(q, "q", 2)
     bs, bp = _u8(bs, "bs", 2)
     n, half = q.shape
@@ -269,5 +349,5 @@ __all__ = [
     "fp8_gemv", "nvfp4_gemv", "fp8_matmul", "nvfp4_matmul", "fp8_grouped_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
     "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
-    "SIGNATURES", "LIB_PATH", "version", "status_str",
+    "SIGNATURES", "LIB_PATH", "version", "status_str", "ACTIVATIONS", "Epilogue",
 ]

@@ -70,7 +70,30 @@ int device_ctx(cudaStream_t stream, Ctx* ctx) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_dtype(int t) { return t == GQ_F32 || t == GQ_BF16; }
+bool valid_dtype(int t) { return t == GQ_F32 || t == GQ_BF16 || t == GQ_F16; }
+
+int out_size(int t) { return t == GQ_F32 ? 4 : 2; }
+
+// Checks an epilogue and builds the kernels' descriptor.  bias_stride is the
+// distance between experts' bias rows (grouped) or 0.
+int make_epi(int out_dtype, const gq_epilogue* e, int64_t bias_stride, Epi* ep) {
+  ep->bias = nullptr;
+  ep->bias_stride = 0;
+  ep->bias_kind = kOutF32;
+  ep->act = kActNone;
+  ep->out_kind = out_dtype == GQ_BF16 ? kOutBf16 : (out_dtype == GQ_F16 ? kOutF16 : kOutF32);
+  if (e == nullptr) return GQ_OK;
+  if (e->activation < GQ_ACT_NONE || e->activation > GQ_ACT_GELU_TANH) return GQ_ERR_EPILOGUE;
+  ep->act = e->activation;
+  if (e->bias != nullptr) {
+    if (!valid_dtype(e->bias_dtype)) return GQ_ERR_EPILOGUE;
+    if (!aligned(e->bias, static_cast<uintptr_t>(out_size(e->bias_dtype)))) return GQ_ERR_ALIGN;
+    ep->bias = e->bias;
+    ep->bias_stride = bias_stride;
+    ep->bias_kind = e->bias_dtype == GQ_BF16 ? kOutBf16 : (e->bias_dtype == GQ_F16 ? kOutF16 : kOutF32);
+  }
+  return GQ_OK;
+}
 
 int launch_status(cudaError_t e) {
   if (e == cudaSuccess) return GQ_OK;
@@ -101,6 +124,8 @@ void* tensor_map_encode_fn() {
 }  // namespace gq
 
 using gq::aligned;
+using gq::make_epi;
+using gq::out_size;
 using gq::valid_dtype;
 
 extern "C" {
@@ -115,6 +140,7 @@ const char* gq_status_str(int s) {
     case GQ_ERR_DEVICE: return "GQ_ERR_DEVICE: current device is not an sm_103 GPU";
     case GQ_ERR_LAUNCH: return "GQ_ERR_LAUNCH: kernel launch failed";
     case GQ_ERR_TOO_LARGE: return "GQ_ERR_TOO_LARGE: a size exceeds what the kernel supports";
+    case GQ_ERR_EPILOGUE: return "GQ_ERR_EPILOGUE: unknown activation or bias dtype";
     default: return "unknown gq status";
   }
 }
@@ -129,48 +155,69 @@ int gq_set_launch_flags(uint32_t flags) {
 
 uint32_t gq_get_launch_flags(void) { return gq::g_launch_flags.load(std::memory_order_relaxed); }
 
-int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w, int64_t N,
-                int64_t K, float alpha, cudaStream_t stream) {
+int gq_fp8_gemv_ex(void* y, int out_dtype, const void* x, const uint8_t* w, int64_t N,
+                   int64_t K, float alpha, const gq_epilogue* epilogue, cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
   if (N < 0 || K < 0) return GQ_ERR_SHAPE;
   if (N == 0) return GQ_OK;
   if (!y || (K > 0 && (!x || !w))) return GQ_ERR_NULL;
-  if (!aligned(x, 2) || !aligned(y, out_dtype == GQ_F32 ? 4 : 2)) return GQ_ERR_ALIGN;
+  if (!aligned(x, 2) || !aligned(y, out_size(out_dtype))) return GQ_ERR_ALIGN;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(gq::launch_fp8_gemv(c, y, out_dtype == GQ_BF16, x, w, N, K, alpha));
+  return gq::launch_status(gq::launch_fp8_gemv(c, y, ep, x, w, N, K, alpha));
 }
 
-int gq_nvfp4_gemv(void* y, int out_dtype, const void* x, const uint8_t* q,
-                  const uint8_t* bs, int64_t N, int64_t K, float alpha,
-                  cudaStream_t stream) {
+int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w, int64_t N, int64_t K,
+                float alpha, cudaStream_t stream) {
+  return gq_fp8_gemv_ex(y, out_dtype, x, w, N, K, alpha, nullptr, stream);
+}
+
+int gq_nvfp4_gemv_ex(void* y, int out_dtype, const void* x, const uint8_t* q, const uint8_t* bs,
+                     int64_t N, int64_t K, float alpha, const gq_epilogue* epilogue,
+                     cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
   if (N < 0 || K < 0 || K % 16 != 0) return GQ_ERR_SHAPE;
   if (N == 0) return GQ_OK;
   if (!y || (K > 0 && (!x || !q || !bs))) return GQ_ERR_NULL;
-  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(y, out_dtype == GQ_F32 ? 4 : 2))
-    return GQ_ERR_ALIGN;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(y, out_size(out_dtype))) return GQ_ERR_ALIGN;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(gq::launch_nvfp4_gemv(c, y, out_dtype == GQ_BF16, x, q, bs, N, K, alpha));
+  return gq::launch_status(gq::launch_nvfp4_gemv(c, y, ep, x, q, bs, N, K, alpha));
 }
 
-int gq_fp8_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* w, int64_t M,
+int gq_nvfp4_gemv(void* y, int out_dtype, const void* x, const uint8_t* q, const uint8_t* bs,
                   int64_t N, int64_t K, float alpha, cudaStream_t stream) {
+  return gq_nvfp4_gemv_ex(y, out_dtype, x, q, bs, N, K, alpha, nullptr, stream);
+}
+
+int gq_fp8_matmul_ex(void* c_out, int out_dtype, const void* a, const uint8_t* w, int64_t M,
+                     int64_t N, int64_t K, float alpha, const gq_epilogue* epilogue,
+                     cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
   if (M < 0 || N < 0 || K < 0 || K % 16 != 0) return GQ_ERR_SHAPE;
   if (M == 0 || N == 0) return GQ_OK;
   if (!c_out || (K > 0 && (!a || !w))) return GQ_ERR_NULL;
   if (!aligned(a, 16) || !aligned(w, 16) || !aligned(c_out, 16)) return GQ_ERR_ALIGN;
   if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(gq::launch_fp8_gemm(c, c_out, out_dtype == GQ_BF16, a, w, M, N, K, alpha));
+  return gq::launch_status(gq::launch_fp8_gemm(c, c_out, ep, a, w, M, N, K, alpha));
 }
 
-int gq_nvfp4_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* q,
-                    const uint8_t* bs, int64_t M, int64_t N, int64_t K, float alpha,
-                    cudaStream_t stream) {
+int gq_fp8_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* w, int64_t M,
+                  int64_t N, int64_t K, float alpha, cudaStream_t stream) {
+  return gq_fp8_matmul_ex(c_out, out_dtype, a, w, M, N, K, alpha, nullptr, stream);
+}
+
+int gq_nvfp4_matmul_ex(void* c_out, int out_dtype, const void* a, const uint8_t* q,
+                       const uint8_t* bs, int64_t M, int64_t N, int64_t K, float alpha,
+                       const gq_epilogue* epilogue, cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
   if (M < 0 || N < 0 || K < 0 || K % 64 != 0) return GQ_ERR_SHAPE;
   if (M == 0 || N == 0) return GQ_OK;
@@ -178,21 +225,31 @@ int gq_nvfp4_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* q,
   if (!aligned(a, 16) || !aligned(q, 16) || !aligned(bs, 4) || !aligned(c_out, 16))
     return GQ_ERR_ALIGN;
   if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(
-      gq::launch_nvfp4_gemm(c, c_out, out_dtype == GQ_BF16, a, q, bs, M, N, K, alpha));
+  return gq::launch_status(gq::launch_nvfp4_gemm(c, c_out, ep, a, q, bs, M, N, K, alpha));
 }
 
-int gq_fp8_grouped_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* w,
-                          const uint32_t* a_offsets, const int32_t* expert_ids,
-                          const float* expert_scales, int64_t G, int64_t E,
-                          int64_t max_rows_per_group, int64_t total_M, int64_t N, int64_t K,
-                          cudaStream_t stream) {
+int gq_nvfp4_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* q,
+                    const uint8_t* bs, int64_t M, int64_t N, int64_t K, float alpha,
+                    cudaStream_t stream) {
+  return gq_nvfp4_matmul_ex(c_out, out_dtype, a, q, bs, M, N, K, alpha, nullptr, stream);
+}
+
+int gq_fp8_grouped_matmul_ex(void* c_out, int out_dtype, const void* a, const uint8_t* w,
+                             const uint32_t* a_offsets, const int32_t* expert_ids,
+                             const float* expert_scales, int64_t G, int64_t E,
+                             int64_t max_rows_per_group, int64_t total_M, int64_t N, int64_t K,
+                             const gq_epilogue* epilogue, cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
   if (G < 0 || E < 0 || max_rows_per_group < 0 || total_M < 0 || N < 0 || K < 0 ||
       K % 16 != 0)
     return GQ_ERR_SHAPE;
+  // An empty sum with a bias would need act(bias) written per active group:
+  // not supported (documented).
+  if (K == 0 && epilogue != nullptr && epilogue->bias != nullptr) return GQ_ERR_SHAPE;
   if (G == 0 || total_M == 0 || N == 0 || max_rows_per_group == 0) return GQ_OK;
   if (!c_out || !a_offsets || !expert_ids || (K > 0 && (!a || (E > 0 && !w))))
     return GQ_ERR_NULL;
@@ -202,11 +259,22 @@ int gq_fp8_grouped_matmul(void* c_out, int out_dtype, const void* a, const uint8
   if (G > 65535 || E > 0x7FFFFFFFLL || total_M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL ||
       K > 0x7FFFFFFFLL)
     return GQ_ERR_TOO_LARGE;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, N, &ep)) return s;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(gq::launch_fp8_grouped_gemm(
-      c, c_out, out_dtype == GQ_BF16, a, w, a_offsets, expert_ids, expert_scales, G, E,
-      max_rows_per_group, total_M, N, K));
+  return gq::launch_status(gq::launch_fp8_grouped_gemm(c, c_out, ep, a, w, a_offsets, expert_ids,
+                                                       expert_scales, G, E, max_rows_per_group,
+                                                       total_M, N, K));
+}
+
+int gq_fp8_grouped_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* w,
+                          const uint32_t* a_offsets, const int32_t* expert_ids,
+                          const float* expert_scales, int64_t G, int64_t E,
+                          int64_t max_rows_per_group, int64_t total_M, int64_t N, int64_t K,
+                          cudaStream_t stream) {
+  return gq_fp8_grouped_matmul_ex(c_out, out_dtype, a, w, a_offsets, expert_ids, expert_scales, G,
+                                  E, max_rows_per_group, total_M, N, K, nullptr, stream);
 }
 
 int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w, int64_t N, int64_t K,
@@ -218,7 +286,8 @@ int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w, int64_t N, in
   if (!aligned(out, 16) || !aligned(w, 16)) return GQ_ERR_ALIGN;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(gq::launch_fp8_materialize(c, out, out_dtype == GQ_BF16, w, N * K));
+  const int kind = out_dtype == GQ_BF16 ? gq::kOutBf16 : (out_dtype == GQ_F16 ? gq::kOutF16 : gq::kOutF32);
+  return gq::launch_status(gq::launch_fp8_materialize(c, out, kind, w, N * K));
 }
 
 int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q, const uint8_t* bs,
@@ -230,8 +299,8 @@ int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q, const uint8
   if (!aligned(out, 16) || !aligned(q, 16)) return GQ_ERR_ALIGN;
   gq::Ctx c;
   if (int s = gq::device_ctx(stream, &c)) return s;
-  return gq::launch_status(
-      gq::launch_nvfp4_materialize(c, out, out_dtype == GQ_BF16, q, bs, N * K / 16));
+  const int kind = out_dtype == GQ_BF16 ? gq::kOutBf16 : (out_dtype == GQ_F16 ? gq::kOutF16 : gq::kOutF32);
+  return gq::launch_status(gq::launch_nvfp4_materialize(c, out, kind, q, bs, N * K / 16));
 }
 
 int gq_device_status(uint32_t* flags, int reset) {

@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "internal.h"
+
 namespace gq {
 
 // Status bits recorded by bounded waits that ran out (see gq_device_status).
@@ -189,6 +191,55 @@ __device__ __forceinline__ uint32_t e2m1x2_b(uint32_t w) {
   return out;
 }
 
+// ------------------------------------------------ output and the epilogue --
+//
+// Every product kernel ends in the same fused epilogue (the optional
+// elementwise (row, col) epilogue of the "Matmul2dFp8" struct page, in the
+// form a linear layer uses):  out = act(alpha * acc + bias[n]), converted to
+// the output type with round-to-nearest-even.
+
+// (Epi and the kOut* / kAct* codes are declared in internal.h.)
+
+__device__ __forceinline__ float epi_bias(const Epi& e, int64_t idx) {
+  if (e.bias_kind == kOutF32) return __ldg(static_cast<const float*>(e.bias) + idx);
+  const uint16_t b = __ldg(static_cast<const unsigned short*>(e.bias) + idx);
+  if (e.bias_kind == kOutBf16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ float epi_act(int act, float v) {
+  switch (act) {
+    case kActRelu: return v > 0.f ? v : (v != v ? v : 0.f);   // NaN stays NaN
+    case kActSilu: return v / (1.f + expf(-v));
+    case kActGeluTanh:
+      return 0.5f * v * (1.f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));
+    default: return v;
+  }
+}
+
+// v = alpha * acc already; adds bias element bias_idx (when there is a bias)
+// and applies the activation.
+__device__ __forceinline__ float epi_apply(const Epi& e, float v, int64_t bias_idx) {
+  if (e.bias != nullptr) v += epi_bias(e, bias_idx);
+  return epi_act(e.act, v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void epi_store(void* out, int64_t idx, int out_kind, float v) {
+  if (out_kind == kOutF32) {
+    static_cast<float*>(out)[idx] = v;
+  } else if (out_kind == kOutBf16) {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
 // ----------------------------------------------------------------- stores --
 
 template <typename OutT> struct OutConv;
@@ -204,6 +255,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Four consecutive outputs at idx (idx a multiple of 4, out 16-byte aligned):
+// one 16-byte (f32) or 8-byte (bf16, f16) store.
+__device__ __forceinline__ void epi_store4(void* out, int64_t idx, int out_kind, float v0, float v1,
+                                           float v2, float v3) {
+  if (out_kind == kOutF32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(v0, v1, v2, v3);
+  } else if (out_kind == kOutBf16) {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+        make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+  } else {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+        make_uint2(pack_f16x2(v0, v1), pack_f16x2(v2, v3));
+  }
 }
 
 // Programmatic dependent launch.  pdl_wait() blocks until the grid this one

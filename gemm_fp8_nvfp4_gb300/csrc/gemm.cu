@@ -112,7 +112,7 @@ struct Problem {
   int num_n_tiles;
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
-  int bf16_out;
+  Epi ep;                      // output type and fused epilogue
   int ksplit;                  // > 1: split-K over a thread-block cluster of ksplit CTAs
   int kb_per_split;            // K steps per split
 };
@@ -460,9 +460,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid) continue;
       if (tl.expert < 0) {
-        // Inactive group: write zeros for its rows, no tensor-core work.
-        const bool vec0 = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
-        const int per16 = p.bf16_out ? 8 : 4;            // elements per 16-byte store
+        // Inactive group: write zeros for its rows (all-zero bits in every
+        // output type; no epilogue), no tensor-core work.
+        const int es = p.ep.out_kind == kOutF32 ? 4 : 2;   // bytes per output element
+        const bool vec0 = (static_cast<int64_t>(p.N) * es) % 16 == 0;
+        const int per16 = 16 / es;                        // elements per 16-byte store
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
@@ -471,14 +473,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0;
           int c = 0;
           if (vec0) {
-            uint4* dst = p.bf16_out ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o)
-                                    : reinterpret_cast<uint4*>(static_cast<float*>(p.out) + o);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + o * es);
             for (; c + per16 <= cend; c += per16) dst[c / per16] = make_uint4(0u, 0u, 0u, 0u);
           }
-          for (; c < cend; ++c) {
-            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + c] = __float2bfloat16_rn(0.f);
-            else static_cast<float*>(p.out)[o + c] = 0.f;
-          }
+          for (; c < cend; ++c) epi_store(p.out, o + c, p.ep.out_kind, 0.f);
         }
         continue;
       }
@@ -510,7 +508,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
         continue;
       }
-      const bool vec_ok = p.bf16_out ? (p.N % 8 == 0) : (p.N % 4 == 0);
+      const bool f32_out = p.ep.out_kind == kOutF32;
+      const bool vec_ok = f32_out ? (p.N % 4 == 0) : (p.N % 8 == 0);
+      const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
       const int halves = tl.m_end - tl.m0 > UMMA_M ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
@@ -524,31 +524,34 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           tc::tmem_wait_ld();
           const int n = tl.n0 + c0;
           if (!row_ok || n >= p.N) continue;
+          const int lim = min(32, p.N - n);
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i)
+            v[i] = epi_apply(p.ep, tl.scale * __uint_as_float(r[i]), bias0 + n + (i < lim ? i : 0));
           const int64_t o = static_cast<int64_t>(m) * p.N + n;
-          if (vec_ok && n + 32 <= p.N) {
-            if (p.bf16_out) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-            } else {
+          if (vec_ok && lim == 32) {
+            if (f32_out) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-            }
-          } else {
-            const int lim = min(32, p.N - n);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o);
+              const bool h16 = p.ep.out_kind == kOutF16;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i < lim) {
-                if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[o + i] = __float2bfloat16_rn(v[i]);
-                else static_cast<float*>(p.out)[o + i] = v[i];
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  w[j] = h16 ? pack_f16x2(v[8 * i + 2 * j], v[8 * i + 2 * j + 1])
+                             : pack_bf16x2(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < lim) epi_store(p.out, o + i, p.ep.out_kind, v[i]);
           }
         }
       }
@@ -585,12 +588,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
         const int64_t base = static_cast<int64_t>(m) * p.N + n;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (n + i < p.N) {
-            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[base + i] = __float2bfloat16_rn(o[i]);
-            else static_cast<float*>(p.out)[base + i] = o[i];
-          }
-        }
+        for (int i = 0; i < 4; ++i)
+          if (n + i < p.N) epi_store(p.out, base + i, p.ep.out_kind, epi_apply(p.ep, o[i], n + i));
       }
     }
     tc::cluster_sync();   // no CTA leaves while a peer still reads its partial
@@ -601,14 +600,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   }
 }
 
-// Writes alpha * 0 (K = 0: the sum is empty).
-__global__ void k_fill_scaled_zero(void* out, int bf16_out, int64_t count, float alpha) {
+// K = 0 (the sum is empty): out[m, n] = epilogue(alpha * 0) for the column n.
+__global__ void k_fill_scaled_zero(void* out, Epi ep, int64_t count, int64_t N, float alpha) {
   const float v = alpha * 0.f;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    if (bf16_out) static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
-    else static_cast<float*>(out)[i] = v;
-  }
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    epi_store(out, i, ep.out_kind, epi_apply(ep, v, i % N));
 }
 
 // --------------------------------------------------------------- host --
@@ -642,13 +639,13 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   return cudaLaunchKernelEx(&cfg, kern, ta, tw, scales, p);
 }
 
-cudaError_t fill_zero(const Ctx& c, void* out, bool bf16_out, int64_t count, float alpha) {
+cudaError_t fill_zero(const Ctx& c, void* out, const Epi& ep, int64_t count, int64_t N, float alpha) {
   const int grid = static_cast<int>(std::min<int64_t>((count + 255) / 256, c.num_sms * 8LL));
-  k_fill_scaled_zero<<<grid > 0 ? grid : 1, 256, 0, c.stream>>>(out, bf16_out ? 1 : 0, count, alpha);
+  k_fill_scaled_zero<<<grid > 0 ? grid : 1, 256, 0, c.stream>>>(out, ep, count, N > 0 ? N : 1, alpha);
   return cudaGetLastError();
 }
 
-Problem base_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_t N, int64_t K,
+Problem base_problem(const Ctx& c, void* out, const Epi& ep, int64_t M, int64_t N, int64_t K,
                      float alpha) {
   Problem p{};
   p.out = out;
@@ -659,7 +656,7 @@ Problem base_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_t 
   p.K = static_cast<int>(K);
   p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
   p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
-  p.bf16_out = bf16_out ? 1 : 0;
+  p.ep = ep;
   p.ksplit = 1;
   p.kb_per_split = p.num_k_blocks;
   return p;
@@ -684,40 +681,40 @@ int plan_split(const Ctx& c, Problem& p, int tiles) {
 
 }  // namespace
 
-cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* a, const uint8_t* w,
+cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* a, const uint8_t* w,
                             int64_t M, int64_t N, int64_t K, float alpha) {
-  if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
-  if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, bf16_out, a, w, M, N, K, alpha);
+  if (K == 0) return fill_zero(c, out, ep, M * N, N, alpha);
+  if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, ep, a, w, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
+  Problem p = base_problem(c, out, ep, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
   const int grid = plan_split(c, p, tiles);
   return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, grid);
 }
 
-cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                               const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N, int64_t K,
                               float alpha) {
-  if (K == 0) return fill_zero(c, out, bf16_out, M * N, alpha);
+  if (K == 0) return fill_zero(c, out, ep, M * N, N, alpha);
   if (M <= skinny_max_rows() && nvfp4_skinny_ok(bs, K))
-    return launch_nvfp4_gemm_skinny(c, out, bf16_out, a, q, bs, M, N, K, alpha);
+    return launch_nvfp4_gemm_skinny(c, out, ep, a, q, bs, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K / 2, N, K / 2, BK / 2, BN,
                  CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
-  Problem p = base_problem(c, out, bf16_out, M, N, K, alpha);
+  Problem p = base_problem(c, out, ep, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
   const int grid = plan_split(c, p, tiles);
   return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid);
 }
 
-cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                                     const uint8_t* w, const uint32_t* a_offsets,
                                     const int32_t* expert_ids, const float* expert_scales,
                                     int64_t G, int64_t E, int64_t max_rows, int64_t total_M,
@@ -734,7 +731,7 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out, cons
         !encode_3d(&tw, w, K, N, E, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
-  Problem p = base_problem(c, out, bf16_out, total_M, N, K, 1.0f);
+  Problem p = base_problem(c, out, ep, total_M, N, K, 1.0f);
   p.a_offsets = a_offsets;
   p.expert_ids = expert_ids;
   p.expert_scales = expert_scales;

@@ -135,7 +135,7 @@ struct SkProblem {
   int m_pad;           // activation rows loaded per stage: M rounded up to 8
   int nkb;             // K steps of BK
   int ksplit;          // cluster size S (power of two, <= kMaxSplit; TN / S >= 16)
-  int bf16_out;
+  Epi ep;              // output type and fused epilogue
   int wp_box;          // inner box (bytes) of the weight prefetch map
 };
 
@@ -418,23 +418,17 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
           }
         }
       }
-      const float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+      const int lim = min(4, p.N - n);
+      float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = epi_apply(p.ep, o[i], n + (i < lim ? i : 0));
       const int64_t base = static_cast<int64_t>(m) * p.N + n;
-      if (vec && n + 4 <= p.N) {
-        if (p.bf16_out) {
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + base) =
-              make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
-        } else {
-          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) = make_float4(o[0], o[1], o[2], o[3]);
-        }
+      if (vec && lim == 4) {
+        epi_store4(p.out, base, p.ep.out_kind, o[0], o[1], o[2], o[3]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (n + i < p.N) {
-            if (p.bf16_out) static_cast<__nv_bfloat16*>(p.out)[base + i] = __float2bfloat16_rn(o[i]);
-            else static_cast<float*>(p.out)[base + i] = o[i];
-          }
-        }
+        for (int i = 0; i < 4; ++i)
+          if (i < lim) epi_store(p.out, base + i, p.ep.out_kind, o[i]);
       }
     }
   }
@@ -568,7 +562,7 @@ cudaError_t launch(const Ctx& c, SkProblem p, const void* a, const uint8_t* w, c
   return launch_tn<F, 128>(c, p, s128, a, w, bs, row_bytes);
 }
 
-SkProblem make_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_t N, int64_t K,
+SkProblem make_problem(const Ctx& c, void* out, const Epi& ep, int64_t M, int64_t N, int64_t K,
                        float alpha) {
   SkProblem p{};
   p.out = out;
@@ -580,7 +574,7 @@ SkProblem make_problem(const Ctx& c, void* out, bool bf16_out, int64_t M, int64_
   p.m_pad = static_cast<int>((M + 7) / 8 * 8);
   p.nkb = static_cast<int>((K + BK - 1) / BK);
   p.ksplit = 1;
-  p.bf16_out = bf16_out ? 1 : 0;
+  p.ep = ep;
   return p;
 }
 
@@ -593,16 +587,16 @@ bool nvfp4_skinny_ok(const uint8_t* bs, int64_t K) {
   return K % 256 == 0 && (reinterpret_cast<uintptr_t>(bs) & 15) == 0;
 }
 
-cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, const Epi& ep, const void* a,
                                    const uint8_t* w, int64_t M, int64_t N, int64_t K, float alpha) {
-  return launch<Fmt::kFp8>(c, make_problem(c, out, bf16_out, M, N, K, alpha), a, w, nullptr, K);
+  return launch<Fmt::kFp8>(c, make_problem(c, out, ep, M, N, K, alpha), a, w, nullptr, K);
 }
 
-cudaError_t launch_nvfp4_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_nvfp4_gemm_skinny(const Ctx& c, void* out, const Epi& ep, const void* a,
                                      const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N,
                                      int64_t K, float alpha) {
   if (!nvfp4_skinny_ok(bs, K)) return cudaErrorInvalidValue;
-  return launch<Fmt::kNvfp4>(c, make_problem(c, out, bf16_out, M, N, K, alpha), a, q, bs, K / 2);
+  return launch<Fmt::kNvfp4>(c, make_problem(c, out, ep, M, N, K, alpha), a, q, bs, K / 2);
 }
 
 }  // namespace gq

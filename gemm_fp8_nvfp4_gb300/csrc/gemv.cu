@@ -136,7 +136,7 @@ __device__ __forceinline__ float fma_fp8(const uint32_t* words, const float* xf,
 
 template <int R, int T>
 __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, int64_t row0,
-                                                 int64_t N, float alpha, void* y, bool bf16_out) {
+                                                 int64_t N, float alpha, void* y, const Epi& ep) {
 #pragma unroll
   for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -155,14 +155,7 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
 #pragma unroll
     for (int wi = 0; wi < T / 32; ++wi) s += red[wi * R + r];
     const int64_t n = row0 + r;
-    if (n < N) {
-      const float v = alpha * s;
-      if (bf16_out) {
-        static_cast<__nv_bfloat16*>(y)[n] = __float2bfloat16_rn(v);
-      } else {
-        static_cast<float*>(y)[n] = v;
-      }
-    }
+    if (n < N) epi_store(y, n, ep.out_kind, epi_apply(ep, alpha * s, n));
   }
 }
 
@@ -170,7 +163,7 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
 
 template <int VEC, int R, int U, int T = kThreads, bool kOverlap = false>
 __global__ void __launch_bounds__(T, 7)   // 7 CTAs per SM (<= 73 registers)
-k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
+k_fp8_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
            const uint8_t* __restrict__ w, int64_t N, int64_t K, float alpha) {
   constexpr int kThreads = T;
   __shared__ float red[(T / 32) * R];
@@ -276,7 +269,7 @@ k_fp8_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
     }
   }
   if (!waited) pdl_wait_ordered();   // threads without a vector still order their store
-  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
+  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, ep);
 }
 
 // ----------------------------------------------------------------- NVFP4 --
@@ -317,7 +310,7 @@ __device__ __forceinline__ void load_xf(const uint16_t* __restrict__ x, int64_t 
 
 template <int VB, int R, int U, int T = kThreads, bool kOverlap = false>
 __global__ void __launch_bounds__(T, 6)   // 6 CTAs per SM (<= 85 registers)
-k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x,
+k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
              const uint8_t* __restrict__ q, const uint8_t* __restrict__ bs, int64_t N,
              int64_t K, float alpha) {
   constexpr int kThreads = T;
@@ -394,43 +387,43 @@ k_nvfp4_gemv(void* __restrict__ y, bool bf16_out, const uint16_t* __restrict__ x
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = acc2[r].x + acc2[r].y;
   if (!waited) pdl_wait_ordered();   // threads without a vector still order their store
-  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, bf16_out);
+  reduce_and_store<R, T>(acc, red, row0, N, alpha, y, ep);
 }
 
 constexpr int kRows = 4;
 
 template <int VEC>
-cudaError_t fp8_dispatch(const Ctx& c, void* y, bool bf16_out, const void* x,
+cudaError_t fp8_dispatch(const Ctx& c, void* y, const Epi& ep, const void* x,
                          const uint8_t* w, int64_t N, int64_t K, float alpha) {
   const int64_t grid = (N + kRows - 1) / kRows;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {
     return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2), kThreads, true>,
-                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
+                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep,
                          static_cast<const uint16_t*>(x), w, N, K, alpha);
   }
   return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, (VEC == 16 ? 4 : 2)>,
-                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out,
+                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep,
                        static_cast<const uint16_t*>(x), w, N, K, alpha);
 }
 
 }  // namespace
 
-cudaError_t launch_fp8_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+cudaError_t launch_fp8_gemv(const Ctx& c, void* y, const Epi& ep, const void* x,
                             const uint8_t* w, int64_t N, int64_t K, float alpha) {
   const uintptr_t wa = reinterpret_cast<uintptr_t>(w);
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
   auto fits = [&](int vec) {
     return K % vec == 0 && wa % vec == 0 && xa % (vec >= 8 ? 16 : 2 * vec) == 0;
   };
-  if (fits(16)) return fp8_dispatch<16>(c, y, bf16_out, x, w, N, K, alpha);
-  if (fits(8)) return fp8_dispatch<8>(c, y, bf16_out, x, w, N, K, alpha);
-  if (fits(4)) return fp8_dispatch<4>(c, y, bf16_out, x, w, N, K, alpha);
-  if (fits(2)) return fp8_dispatch<2>(c, y, bf16_out, x, w, N, K, alpha);
-  return fp8_dispatch<1>(c, y, bf16_out, x, w, N, K, alpha);
+  if (fits(16)) return fp8_dispatch<16>(c, y, ep, x, w, N, K, alpha);
+  if (fits(8)) return fp8_dispatch<8>(c, y, ep, x, w, N, K, alpha);
+  if (fits(4)) return fp8_dispatch<4>(c, y, ep, x, w, N, K, alpha);
+  if (fits(2)) return fp8_dispatch<2>(c, y, ep, x, w, N, K, alpha);
+  return fp8_dispatch<1>(c, y, ep, x, w, N, K, alpha);
 }
 
-cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, const Epi& ep, const void* x,
                               const uint8_t* q, const uint8_t* bs, int64_t N,
                               int64_t K, float alpha) {
   const uint16_t* xb = static_cast<const uint16_t*>(x);
@@ -441,11 +434,11 @@ cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* 
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {
     return launch_kernel(c, true, k_nvfp4_gemv<8, kRows, 2, kThreads, true>,
-                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
+                         dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep, xb, q,
                          bs, N, K, alpha);
   }
   return launch_kernel(c, true, k_nvfp4_gemv<8, kRows, 2>,
-                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, bf16_out, xb, q,
+                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep, xb, q,
                        bs, N, K, alpha);
 }
 

@@ -9,6 +9,19 @@
 
 namespace gq {
 
+// Output type and fused epilogue of a product kernel:
+//   out = act(alpha * acc + bias[n]) converted to out_kind (round to nearest even).
+enum : int { kOutF32 = 0, kOutBf16 = 1, kOutF16 = 2 };
+enum : int { kActNone = 0, kActRelu = 1, kActSilu = 2, kActGeluTanh = 3 };
+
+struct Epi {
+  const void* bias;      // [N] (grouped: [E, N], row e for expert e), or nullptr
+  int64_t bias_stride;   // elements between experts' bias rows (grouped), else 0
+  int bias_kind;         // element type of bias: kOutF32 / kOutBf16 / kOutF16
+  int act;               // kAct*
+  int out_kind;          // kOut*
+};
+
 // Per-call launch context filled by the C-ABI layer.
 struct Ctx {
   cudaStream_t stream;
@@ -39,27 +52,27 @@ cudaError_t launch_kernel(const Ctx& c, bool pdl, void (*kern)(KArgs...), dim3 g
 }
 
 // materialize.cu
-cudaError_t launch_fp8_materialize(const Ctx& c, void* out, bool bf16_out,
+cudaError_t launch_fp8_materialize(const Ctx& c, void* out, int out_kind,
                                    const uint8_t* w, int64_t total);
-cudaError_t launch_nvfp4_materialize(const Ctx& c, void* out, bool bf16_out,
+cudaError_t launch_nvfp4_materialize(const Ctx& c, void* out, int out_kind,
                                      const uint8_t* q, const uint8_t* bs,
                                      int64_t total_blocks);
 
 // gemv.cu
-cudaError_t launch_fp8_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+cudaError_t launch_fp8_gemv(const Ctx& c, void* y, const Epi& ep, const void* x,
                             const uint8_t* w, int64_t N, int64_t K, float alpha);
-cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, bool bf16_out, const void* x,
+cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, const Epi& ep, const void* x,
                               const uint8_t* q, const uint8_t* bs, int64_t N,
                               int64_t K, float alpha);
 
 // gemm.cu
-cudaError_t launch_fp8_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                             const uint8_t* w, int64_t M, int64_t N, int64_t K,
                             float alpha);
-cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                               const uint8_t* q, const uint8_t* bs, int64_t M,
                               int64_t N, int64_t K, float alpha);
-cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out,
+cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                     const void* a, const uint8_t* w,
                                     const uint32_t* a_offsets,
                                     const int32_t* expert_ids,
@@ -70,10 +83,10 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, bool bf16_out,
 // gemm_skinny.cu (M <= skinny_max_rows())
 int skinny_max_rows();
 bool nvfp4_skinny_ok(const uint8_t* bs, int64_t K);   // the NVFP4 few-row kernel takes this K
-cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_fp8_gemm_skinny(const Ctx& c, void* out, const Epi& ep, const void* a,
                                    const uint8_t* w, int64_t M, int64_t N, int64_t K,
                                    float alpha);
-cudaError_t launch_nvfp4_gemm_skinny(const Ctx& c, void* out, bool bf16_out, const void* a,
+cudaError_t launch_nvfp4_gemm_skinny(const Ctx& c, void* out, const Epi& ep, const void* a,
                                      const uint8_t* q, const uint8_t* bs, int64_t M,
                                      int64_t N, int64_t K, float alpha);
 

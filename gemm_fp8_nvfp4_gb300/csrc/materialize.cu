@@ -19,7 +19,26 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <bool kBf16>
+// 16 consecutive values at element idx (16 * sizeof(out type) bytes,
+// 16-byte aligned): float32, bfloat16 or binary16 (all exact here).
+template <int kOut>
+__device__ __forceinline__ void store16(void* out, int64_t idx, const float (&v)[16]) {
+  if constexpr (kOut == kOutF32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = kOut == kOutBf16 ? pack_bf16x2(v[2 * i], v[2 * i + 1]) : pack_f16x2(v[2 * i], v[2 * i + 1]);
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + idx);
+    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+template <int kOut>
 __global__ void __launch_bounds__(kThreads)
 k_fp8_materialize(void* __restrict__ out, const uint8_t* __restrict__ w, int64_t total) {
   const int64_t groups = total / 16;
@@ -38,33 +57,18 @@ k_fp8_materialize(void* __restrict__ out, const uint8_t* __restrict__ w, int64_t
       v[4 * i + 2] = hi.x;
       v[4 * i + 3] = hi.y;
     }
-    if constexpr (kBf16) {
-      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + g * 16);
-      o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-      o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
-                        pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
-    } else {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + g * 16);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
+    store16<kOut>(out, g * 16, v);
   }
   // Tail: the last total % 16 elements, one per thread of block 0.
   if (blockIdx.x == 0) {
     const int64_t t = groups * 16 + threadIdx.x;
     if (t < total) {
-      const float v = e4m3_to_f32(w[t]);
-      if constexpr (kBf16) {
-        static_cast<__nv_bfloat16*>(out)[t] = __float2bfloat16_rn(v);
-      } else {
-        static_cast<float*>(out)[t] = v;
-      }
+      epi_store(out, t, kOut, e4m3_to_f32(w[t]));
     }
   }
 }
 
-template <bool kBf16>
+template <int kOut>
 __global__ void __launch_bounds__(kThreads)
 k_nvfp4_materialize(void* __restrict__ out, const uint8_t* __restrict__ q,
                     const uint8_t* __restrict__ bs, int64_t blocks) {
@@ -84,17 +88,7 @@ k_nvfp4_materialize(void* __restrict__ out, const uint8_t* __restrict__ q,
         v[8 * i + 2 * j + 1] = e.y * scale;
       }
     }
-    if constexpr (kBf16) {
-      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + b * 16);
-      o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-      o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
-                        pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
-    } else {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + b * 16);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    }
+    store16<kOut>(out, b * 16, v);
   }
 }
 
@@ -106,26 +100,25 @@ int grid_for(int64_t items, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_fp8_materialize(const Ctx& c, void* out, bool bf16_out,
+cudaError_t launch_fp8_materialize(const Ctx& c, void* out, int out_kind,
                                    const uint8_t* w, int64_t total) {
   const int grid = grid_for(total / 16 > 0 ? total / 16 : 1, c.num_sms);
-  if (bf16_out) {
-    k_fp8_materialize<true><<<grid, kThreads, 0, c.stream>>>(out, w, total);
-  } else {
-    k_fp8_materialize<false><<<grid, kThreads, 0, c.stream>>>(out, w, total);
-  }
+  if (out_kind == kOutBf16) k_fp8_materialize<kOutBf16><<<grid, kThreads, 0, c.stream>>>(out, w, total);
+  else if (out_kind == kOutF16) k_fp8_materialize<kOutF16><<<grid, kThreads, 0, c.stream>>>(out, w, total);
+  else k_fp8_materialize<kOutF32><<<grid, kThreads, 0, c.stream>>>(out, w, total);
   return cudaGetLastError();
 }
 
-cudaError_t launch_nvfp4_materialize(const Ctx& c, void* out, bool bf16_out,
+cudaError_t launch_nvfp4_materialize(const Ctx& c, void* out, int out_kind,
                                      const uint8_t* q, const uint8_t* bs,
                                      int64_t total_blocks) {
   const int grid = grid_for(total_blocks, c.num_sms);
-  if (bf16_out) {
-    k_nvfp4_materialize<true><<<grid, kThreads, 0, c.stream>>>(out, q, bs, total_blocks);
-  } else {
-    k_nvfp4_materialize<false><<<grid, kThreads, 0, c.stream>>>(out, q, bs, total_blocks);
-  }
+  if (out_kind == kOutBf16)
+    k_nvfp4_materialize<kOutBf16><<<grid, kThreads, 0, c.stream>>>(out, q, bs, total_blocks);
+  else if (out_kind == kOutF16)
+    k_nvfp4_materialize<kOutF16><<<grid, kThreads, 0, c.stream>>>(out, q, bs, total_blocks);
+  else
+    k_nvfp4_materialize<kOutF32><<<grid, kThreads, 0, c.stream>>>(out, q, bs, total_blocks);
   return cudaGetLastError();
 }
 

@@ -24,8 +24,9 @@
  *   - Work is queued on `stream` (0 = the legacy default stream); the call does
  *     not synchronize.  Argument checks run on the host before anything is
  *     queued; a non-zero status means nothing was queued.
- *   - Activations are bfloat16 bit patterns.  Outputs are float32 or bfloat16
- *     (`out_dtype`), converted from the fp32 result with round-to-nearest-even.
+ *   - Activations are bfloat16 bit patterns.  Outputs are float32, bfloat16 or
+ *     binary16 (`out_dtype`; the "Matmul2dFp8" struct page lists the same three
+ *     for c_type), converted from the fp32 result with round-to-nearest-even.
  *   - `alpha` multiplies the fp32 sum once, before the output conversion
  *     (alpha = 1 gives the raw product).  Because a scalar factors out of the
  *     sum this equals folding the scale after the matmul.
@@ -33,7 +34,7 @@
  *     activations, outputs); block scales need 1 byte.  Odd K is allowed for
  *     the FP8 GEMV (it picks a narrower load width); see each call.
  *   - Zero-sized M or N: nothing is queued, GQ_OK.  K = 0: outputs are written
- *     as alpha * 0.
+ *     as alpha * 0 (through the epilogue, when there is one).
  *   - Results are deterministic: a given call on given inputs returns the same
  *     bits every time (fixed summation order, no atomics).
  *   - Every wait inside the kernels is bounded; a wait that runs out records a
@@ -58,23 +59,62 @@ typedef enum {
   GQ_ERR_DTYPE = 4,     /* unknown output dtype                               */
   GQ_ERR_DEVICE = 5,    /* current device is not sm_103 or cannot be queried  */
   GQ_ERR_LAUNCH = 6,    /* the kernel launch failed (cudaGetLastError)        */
-  GQ_ERR_TOO_LARGE = 7  /* a size exceeds what the kernel supports            */
+  GQ_ERR_TOO_LARGE = 7, /* a size exceeds what the kernel supports            */
+  GQ_ERR_EPILOGUE = 8   /* unknown activation or bias dtype in a gq_epilogue  */
 } gq_status;
 
-typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
+typedef enum { GQ_F32 = 0, GQ_BF16 = 1, GQ_F16 = 2 } gq_dtype;
+
+/*
+ * Fused epilogue (the optional elementwise epilogue of the tiled matmul,
+ * "Matmul2dFp8" struct page, parameter elementwise_lambda_fn: a function of
+ * the output coordinate (row, col) and the computed value, applied where the
+ * result is stored).  The C ABI takes the form a linear layer uses:
+ *
+ *     out[m, n] = act(alpha * acc[m, n] + bias[n])
+ *
+ * then the output conversion.  The grouped product takes a bias row per
+ * expert: bias[e, n] for the rows of a group whose expert is e (rows of a
+ * group with expert id -1 stay zero, no epilogue).
+ *   bias        device pointer to N elements ([E, N] for the grouped call) of
+ *               type bias_dtype (GQ_F32, GQ_BF16 or GQ_F16), aligned to the
+ *               element size; NULL for no bias.
+ *   activation  GQ_ACT_NONE, GQ_ACT_RELU (max(v, 0); NaN stays NaN),
+ *               GQ_ACT_SILU (v / (1 + exp(-v))) or GQ_ACT_GELU_TANH
+ *               (0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))), evaluated in
+ *               fp32 with the CUDA math library.
+ * A NULL gq_epilogue pointer is the plain product (no bias, no activation).
+ * Unknown codes return GQ_ERR_EPILOGUE; a misaligned bias GQ_ERR_ALIGN.
+ */
+typedef enum {
+  GQ_ACT_NONE = 0,
+  GQ_ACT_RELU = 1,
+  GQ_ACT_SILU = 2,
+  GQ_ACT_GELU_TANH = 3
+} gq_activation;
+
+typedef struct gq_epilogue {
+  const void* bias;
+  int bias_dtype;
+  int activation;
+} gq_epilogue;
 
 /*
  * Process-wide launch options (default 0).
  *
- * GQ_LAUNCH_OVERLAP_WEIGHT_READS: the GEMV entry points (gq_fp8_gemv,
- * gq_nvfp4_gemv) launch their kernel as a programmatic dependent of the
- * previous kernel in the stream.  Each thread issues its first weight loads
- * immediately and waits for the previous kernel to finish (and its writes to
- * become visible) before it reads x or writes y.  The weight stream of a GEMV
- * then overlaps the tail of the kernel before it, which is what a decode loop
- * over layers with fixed weights wants.  Only set it when no kernel issued
- * just before a GEMV writes that GEMV's weight buffers: those reads are not
- * ordered after the previous kernel.  Activations and outputs always are.
+ * The GEMV entry points (gq_fp8_gemv, gq_nvfp4_gemv and their _ex forms)
+ * always launch their kernel as a programmatic dependent of the previous
+ * kernel in the stream; by default every thread waits for that kernel to
+ * finish (and its writes to become visible) before it touches any global
+ * memory, so stream order is unchanged and only the launch gap is hidden.
+ *
+ * GQ_LAUNCH_OVERLAP_WEIGHT_READS: each GEMV thread issues its first weight
+ * loads before that wait, and reads x and writes y only after it.  The weight
+ * stream of a GEMV then overlaps the tail of the kernel before it, which is
+ * what a decode loop over layers with fixed weights wants.  Only set it when
+ * no kernel issued just before a GEMV writes that GEMV's weight buffers:
+ * those reads are not ordered after the previous kernel.  Activations and
+ * outputs always are.
  * Not a citation of the pages: a GB300 launch option.
  * gq_set_launch_flags returns GQ_ERR_SHAPE for unknown bits.
  */
@@ -92,7 +132,7 @@ const char* gq_version(void);
  * FP8 GEMV (M = 1 decode).  y[n] = alpha * sum_k x[k] * e4m3(w[n, k]).
  * Source: "fp8_gemv" page -- enqueue_apple_fp8_gemv and fp8_gemv_kernel (one
  * warp per output, lanes striding K, fp32 FMA, warp sum, narrow tail).
- *   y      [N]    float32 or bfloat16 (out_dtype)
+ *   y      [N]    out_dtype
  *   x      [K]    bfloat16
  *   w      [N, K] float8_e4m3fn codes
  * Any K >= 0.  Pointer alignment: 16 bytes gives the widest loads; less is
@@ -100,6 +140,10 @@ const char* gq_version(void);
  */
 int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w,
                 int64_t N, int64_t K, float alpha, cudaStream_t stream);
+/* The same with a fused epilogue (see gq_epilogue; NULL = gq_fp8_gemv). */
+int gq_fp8_gemv_ex(void* y, int out_dtype, const void* x, const uint8_t* w,
+                   int64_t N, int64_t K, float alpha, const gq_epilogue* epilogue,
+                   cudaStream_t stream);
 
 /*
  * NVFP4 GEMV (M = 1).  y[n] = alpha * sum_k x[k] * e2m1(q[n, k]) * e4m3(bs[n, k/16]).
@@ -112,6 +156,10 @@ int gq_fp8_gemv(void* y, int out_dtype, const void* x, const uint8_t* w,
 int gq_nvfp4_gemv(void* y, int out_dtype, const void* x, const uint8_t* q,
                   const uint8_t* bs, int64_t N, int64_t K, float alpha,
                   cudaStream_t stream);
+/* The same with a fused epilogue (see gq_epilogue; NULL = gq_nvfp4_gemv). */
+int gq_nvfp4_gemv_ex(void* y, int out_dtype, const void* x, const uint8_t* q,
+                     const uint8_t* bs, int64_t N, int64_t K, float alpha,
+                     const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
  * FP8 GEMM (M >= 1).  c[m, n] = alpha * sum_k a[m, k] * e4m3(w[n, k]).
@@ -124,6 +172,10 @@ int gq_nvfp4_gemv(void* y, int out_dtype, const void* x, const uint8_t* q,
 int gq_fp8_matmul(void* c, int out_dtype, const void* a, const uint8_t* w,
                   int64_t M, int64_t N, int64_t K, float alpha,
                   cudaStream_t stream);
+/* The same with a fused epilogue (see gq_epilogue; NULL = gq_fp8_matmul). */
+int gq_fp8_matmul_ex(void* c, int out_dtype, const void* a, const uint8_t* w,
+                     int64_t M, int64_t N, int64_t K, float alpha,
+                     const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
  * NVFP4 GEMM (M >= 1).  c = alpha * a @ dequant(q, bs)^T.
@@ -136,6 +188,10 @@ int gq_fp8_matmul(void* c, int out_dtype, const void* a, const uint8_t* w,
 int gq_nvfp4_matmul(void* c, int out_dtype, const void* a, const uint8_t* q,
                     const uint8_t* bs, int64_t M, int64_t N, int64_t K,
                     float alpha, cudaStream_t stream);
+/* The same with a fused epilogue (see gq_epilogue; NULL = gq_nvfp4_matmul). */
+int gq_nvfp4_matmul_ex(void* c, int out_dtype, const void* a, const uint8_t* q,
+                       const uint8_t* bs, int64_t M, int64_t N, int64_t K,
+                       float alpha, const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
  * Grouped (MoE) FP8 GEMM.  For every group z in [0, G):
@@ -166,10 +222,18 @@ int gq_fp8_grouped_matmul(void* c, int out_dtype, const void* a,
                           int64_t G, int64_t E, int64_t max_rows_per_group,
                           int64_t total_M, int64_t N, int64_t K,
                           cudaStream_t stream);
+/* The same with a fused epilogue; its bias is [E, N] (row e for expert e).
+ * K = 0 with a bias returns GQ_ERR_SHAPE.  NULL = gq_fp8_grouped_matmul. */
+int gq_fp8_grouped_matmul_ex(void* c, int out_dtype, const void* a,
+                             const uint8_t* w, const uint32_t* a_offsets,
+                             const int32_t* expert_ids, const float* expert_scales,
+                             int64_t G, int64_t E, int64_t max_rows_per_group,
+                             int64_t total_M, int64_t N, int64_t K,
+                             const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
- * FP8 materialize: out[n, k] = e4m3(w[n, k]) as float32 or bfloat16, exact
- * (every E4M3 value is representable in both), no scale applied.
+ * FP8 materialize: out[n, k] = e4m3(w[n, k]) as float32, bfloat16 or binary16,
+ * exact (every E4M3 value is representable in all three), no scale applied.
  * Source: "fp8_gemv" page -- enqueue_fp8_materialize / fp8_materialize_kernel.
  *   out [N, K] (out_dtype), w [N, K].
  */
@@ -178,8 +242,8 @@ int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w,
 
 /*
  * NVFP4 materialize: out[n, k] = e2m1(q[n, k]) * e4m3(bs[n, k/16]), exact in
- * float32 and bfloat16 (the product has at most 6 significant bits), no
- * per-tensor scale applied.  Source: "fp4_matmul" page (weight layout); the
+ * float32, bfloat16 and binary16 (the product has at most 6 significant bits
+ * and lies in [2^-10, 2688]), no per-tensor scale applied.  Source: "fp4_matmul" page (weight layout); the
  * NVFP4 counterpart of the FP8 materialize.
  *   out [N, K] (out_dtype), q [N, K/2], bs [N, K/16].  K % 16 == 0.
  */

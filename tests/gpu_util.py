@@ -20,10 +20,13 @@ def lib():
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
-    """GPU output (float32 or bf16) -> float64 numpy, exactly."""
+    """GPU output (float32, bf16 or f16) -> float64 numpy, exactly (the 16-bit
+    types decoded from their bit patterns by the oracle's format code)."""
     t = t.detach().to("cpu")
     if t.dtype == torch.bfloat16:
         return oracle.bf16_bits_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    if t.dtype == torch.float16:
+        return oracle.f16_bits_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
     return t.to(torch.float64).numpy()
 
 

@@ -49,7 +49,7 @@ def test_binding_declares_every_symbol(lib_path):
 def test_status_strings(lib_path):
     import gemm_fp8_nvfp4_gb300 as gq
     gq.load_library(lib_path)
-    for s in range(8):
+    for s in range(9):
         assert gq.status_str(s).startswith("GQ_")
     assert "unknown" in gq.status_str(99)
 
