@@ -217,11 +217,23 @@ __device__ __forceinline__ float epi_act(int act, float v) {
   }
 }
 
+// The activation as an out-of-line call: kernels apply the epilogue at many
+// unrolled sites, and inlining the transcendental code at each would bloat
+// the code that every warp role of a persistent kernel shares.
+static __device__ __noinline__ float epi_act_call(int act, float v) { return epi_act(act, v); }
+
+// True when the epilogue is the identity (no bias, no activation): kernels
+// test it once per chunk of outputs and skip epi_apply.
+__device__ __forceinline__ bool epi_plain(const Epi& e) {
+  return e.bias == nullptr && e.act == kActNone;
+}
+
 // v = alpha * acc already; adds bias element bias_idx (when there is a bias)
 // and applies the activation.
 __device__ __forceinline__ float epi_apply(const Epi& e, float v, int64_t bias_idx) {
   if (e.bias != nullptr) v += epi_bias(e, bias_idx);
-  return epi_act(e.act, v);
+  if (e.act != kActNone) v = epi_act_call(e.act, v);
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

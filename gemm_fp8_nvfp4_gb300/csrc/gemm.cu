@@ -508,8 +508,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
         continue;
       }
-      const bool f32_out = p.ep.out_kind == kOutF32;
-      const bool vec_ok = f32_out ? (p.N % 4 == 0) : (p.N % 8 == 0);
+      const bool plain_epi = epi_plain(p.ep);
+      const bool vec_ok = p.ep.out_kind == kOutF32 ? (p.N % 4 == 0) : (p.N % 8 == 0);
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
       const int halves = tl.m_end - tl.m0 > UMMA_M ? 2 : 1;
 #pragma unroll 1
@@ -527,26 +527,29 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           const int lim = min(32, p.N - n);
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            v[i] = epi_apply(p.ep, tl.scale * __uint_as_float(r[i]), bias0 + n + (i < lim ? i : 0));
+          for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+          if (!plain_epi) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = epi_apply(p.ep, v[i], bias0 + n + (i < lim ? i : 0));
+          }
           const int64_t o = static_cast<int64_t>(m) * p.N + n;
           if (vec_ok && lim == 32) {
-            if (f32_out) {
+            if (p.ep.out_kind == kOutF32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            } else if (p.ep.out_kind == kOutBf16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
             } else {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o);
-              const bool h16 = p.ep.out_kind == kOutF16;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  w[j] = h16 ? pack_f16x2(v[8 * i + 2 * j], v[8 * i + 2 * j + 1])
-                             : pack_bf16x2(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_f16x2(v[8 * i], v[8 * i + 1]), pack_f16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_f16x2(v[8 * i + 4], v[8 * i + 5]), pack_f16x2(v[8 * i + 6], v[8 * i + 7]));
             }
           } else {
 #pragma unroll
