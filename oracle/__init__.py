@@ -42,6 +42,7 @@ from .layer import (
     nvfp4_gemv,
     nvfp4_matmul,
     fp8_grouped_matmul,
+    nvfp4_grouped_matmul,
     fp8_materialize,
     nvfp4_materialize,
     abs_dot,
@@ -58,7 +59,7 @@ __all__ = [
     "e4m3_table", "e2m1_table", "bf16_bits_to_f64", "f64_to_bf16_bits",
     "decode_fp8", "decode_nvfp4", "nibble",
     "linear", "linear_loops", "fp8_gemv", "fp8_matmul", "nvfp4_gemv",
-    "nvfp4_matmul", "fp8_grouped_matmul", "fp8_materialize",
+    "nvfp4_matmul", "fp8_grouped_matmul", "nvfp4_grouped_matmul", "fp8_materialize",
     "nvfp4_materialize", "abs_dot", "bf16_ulp", "tolerance",
     "f16_bits_to_f64", "f64_to_f16_bits", "f16_ulp", "activation", "ACT_LIPSCHITZ",
     "epilogue", "tolerance_epilogue",

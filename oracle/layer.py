@@ -87,23 +87,9 @@ def nvfp4_matmul(a, q_packed, block_scales, alpha=1.0) -> np.ndarray:
     return linear(a, decode_nvfp4(q_packed, block_scales), alpha)
 
 
-def fp8_grouped_matmul(a, w_stack, a_offsets, expert_ids, expert_scales=None,
-                       rows=None):
-    """Grouped (MoE) FP8 product.
-
-    a:             [total_M, K] activations (bf16 bits or float values)
-    w_stack:       uint8 [E, N, K] e4m3 codes, one weight per expert
-    a_offsets:     [G + 1] row offsets; group z owns rows a_offsets[z] .. a_offsets[z+1]-1
-    expert_ids:    [G] expert of each group; -1 marks a group that writes zeros
-    expert_scales: [E] per-expert scale folded after the product, or None (raw)
-    rows:          optional sorted array of row indices to compute (others are
-                   left NaN); used to check a few rows of a large problem.
-
-    Returns (out [total_M, N] float64, written [total_M] bool).  Rows that no
-    group covers are NaN and not marked written.
-    """
-    w_stack = np.asarray(w_stack, dtype=np.uint8)
-    n_experts, n_cols, _ = w_stack.shape
+def _grouped(a, n_experts, n_cols, decode_expert, a_offsets, expert_ids, expert_scales, rows):
+    """The grouped loop of ``run_grouped``, with the weight of expert e given by
+    decode_expert(e) (float64 [N, K])."""
     offs = [int(v) for v in np.asarray(a_offsets).reshape(-1)]
     ids = [int(v) for v in np.asarray(expert_ids).reshape(-1)]
     a_arr = np.asarray(a)
@@ -128,11 +114,44 @@ def fp8_grouped_matmul(a, w_stack, a_offsets, expert_ids, expert_scales=None,
             out[sel, :] = 0.0             # inactive group writes zeros
         else:
             if expert not in decoded:
-                decoded[expert] = decode_fp8(w_stack[expert])
+                decoded[expert] = decode_expert(expert)
             scale = 1.0 if expert_scales is None else float(np.asarray(expert_scales)[expert])
             out[sel, :] = linear(a_arr[sel], decoded[expert], scale)
         written[start:stop] = True
     return out, written
+
+
+def fp8_grouped_matmul(a, w_stack, a_offsets, expert_ids, expert_scales=None,
+                       rows=None):
+    """Grouped (MoE) FP8 product.
+
+    a:             [total_M, K] activations (bf16 bits or float values)
+    w_stack:       uint8 [E, N, K] e4m3 codes, one weight per expert
+    a_offsets:     [G + 1] row offsets; group z owns rows a_offsets[z] .. a_offsets[z+1]-1
+    expert_ids:    [G] expert of each group; -1 marks a group that writes zeros
+    expert_scales: [E] per-expert scale folded after the product, or None (raw)
+    rows:          optional sorted array of row indices to compute (others are
+                   left NaN); used to check a few rows of a large problem.
+
+    Returns (out [total_M, N] float64, written [total_M] bool).  Rows that no
+    group covers are NaN and not marked written.
+    """
+    w_stack = np.asarray(w_stack, dtype=np.uint8)
+    n_experts, n_cols, _ = w_stack.shape
+    return _grouped(a, n_experts, n_cols, lambda e: decode_fp8(w_stack[e]), a_offsets,
+                    expert_ids, expert_scales, rows)
+
+
+def nvfp4_grouped_matmul(a, q_stack, bs_stack, a_offsets, expert_ids, expert_scales=None,
+                         rows=None):
+    """Grouped (MoE) NVFP4 product: the same groups as ``fp8_grouped_matmul``
+    with expert e's weight the NVFP4 pair q_stack[e] (uint8 [N, K/2]) and
+    bs_stack[e] (uint8 [N, K/16]); expert_scales[e] is its second scale."""
+    q_stack = np.asarray(q_stack, dtype=np.uint8)
+    bs_stack = np.asarray(bs_stack, dtype=np.uint8)
+    n_experts, n_cols, _ = q_stack.shape
+    return _grouped(a, n_experts, n_cols, lambda e: decode_nvfp4(q_stack[e], bs_stack[e]),
+                    a_offsets, expert_ids, expert_scales, rows)
 
 
 def fp8_materialize(w_codes) -> np.ndarray:

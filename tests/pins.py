@@ -468,11 +468,59 @@ def check_epilogue(orc):
     assert t16[0] == 3.0 * 2.0 ** -20 + 2.0 ** -9      # f16 ulp on [2, 4) is 2^-9
 
 
+def check_nvfp4_grouped_worked(orc):
+    rows = _rows("nvfp4_grouped_worked.txt")
+    q = np.zeros((2, 2, 8), dtype=np.uint8)
+    bs = np.zeros((2, 2, 1), dtype=np.uint8)
+    for e in range(2):
+        q[e] = [[int(c, 16) for c in r] for r in rows[f"q{e}"]]
+        bs[e] = [[int(c, 16) for c in r] for r in rows[f"bs{e}"]]
+    scales = np.array([float(v) for v in rows["scales"][0]])
+    offs = np.array([int(v) for v in rows["a_offsets"][0]])
+    ids = np.array([int(v) for v in rows["expert_ids"][0]])
+    a = np.array([[float(v) for v in r] for r in rows["a"]])
+    want = np.array([[float(v) for v in r] for r in rows["out"]])
+    got, written = orc.nvfp4_grouped_matmul(a, q, bs, offs, ids, scales)
+    assert written.all()
+    assert np.array_equal(got, want), got
+
+
+def check_nvfp4_grouped_vs_dense(orc, seed=17):
+    """NVFP4 grouped equals, row by row, the second scale times the product
+    with an independent element-by-element decode of the expert's weight;
+    -1 and unknown ids give zeros, uncovered rows stay unwritten."""
+    rng = np.random.default_rng(seed)
+    e, n, k = 3, 4, 32
+    q = rng.integers(0, 256, size=(e, n, k // 2), dtype=np.uint8)
+    bs = rng.integers(0, 0x7F, size=(e, n, k // 16), dtype=np.uint8)
+    scales = np.array([0.25, 2.0, 1.5])
+    offs = np.array([1, 3, 3, 6, 8])
+    ids = np.array([2, 0, -1, 5])
+    bits, _ = _bf16_values(rng, (9, k))
+    got, written = orc.nvfp4_grouped_matmul(bits, q, bs, offs, ids, scales)
+    assert not written[0] and not written[8]
+    t4 = golden_e2m1()
+    xv = orc.bf16_bits_to_f64(bits)
+    for z, ex in enumerate(ids):
+        for r in range(offs[z], offs[z + 1]):
+            if ex == -1 or not (0 <= ex < e):
+                assert np.all(got[r] == 0.0)
+                continue
+            sv = torch_e4m3(bs[ex])
+            for col in range(n):
+                acc = 0.0
+                for c in range(k):
+                    byte = int(q[ex, col, c // 2])
+                    code = (byte & 0xF) if c % 2 == 0 else (byte >> 4)
+                    acc += xv[r, c] * t4[code] * float(sv[col, c // 16])
+                assert np.isclose(got[r, col], scales[ex] * acc, rtol=1e-12, atol=1e-300)
+
+
 ALL_CHECKS = [
     check_e4m3_table, check_e2m1_table, check_bf16_exactness, check_bf16_rounding,
     check_bf16_decode, check_fp8_worked, check_nvfp4_worked, check_grouped_worked,
     check_bruteforce_fp8, check_bruteforce_nvfp4, check_nvfp4_materialize_independent,
     check_fp8_materialize_independent, check_scale_fold, check_gemv_is_gemm_row,
     check_grouped_vs_dense, check_tolerance_shape, check_f16_decode, check_f16_rounding,
-    check_activations, check_epilogue,
+    check_activations, check_epilogue, check_nvfp4_grouped_worked, check_nvfp4_grouped_vs_dense,
 ]
