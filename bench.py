@@ -477,7 +477,7 @@ def gemm_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
 
 
 def grouped_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
-    """Grouped MoE FP8: 8 experts [8, 14336, 4096], 4096 routed rows."""
+    """Grouped MoE, FP8 then NVFP4: 8 experts [8, 14336, 4096], 4096 routed rows."""
     import synth
     stack, scales = synth.fp8_expert_stack(8, 14336, 4096, seed=0)
     a = synth.bf16_activations(4096, 4096, seed=1)
@@ -499,6 +499,23 @@ def grouped_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
                                "frac_bf16_tensor": round(tfl / peaks["bf16_tflops"], 4),
                                "active_rows": active_rows,
                                "l2": "weights 470 MB > L2"}
+    del d_stack
+
+    # The same routing with NVFP4 experts (q [8, 14336, 2048], bs [8, 14336, 256]).
+    q, bs, s2 = synth.nvfp4_expert_stack(8, 14336, 4096, seed=0)
+    d_q, d_bs, d_s2 = q.to(dev), bs.to(dev), s2.to(dev)
+
+    def nvfp4_grouped_step(i):
+        gq.nvfp4_grouped_matmul(d_a, d_q, d_bs, d_offs, d_ids, d_s2,
+                                max_rows_per_group=int(counts.max()), out=outg, stream=stream)
+
+    ms = graph_timer(nvfp4_grouped_step, gsteps, warm, gsteps, stream, world)
+    t = ms * 1e-3 / gsteps
+    tfl = 2 * 14336 * 4096 * active_rows / t / 1e12
+    subs["nvfp4_grouped_moe"] = {"us_per_launch": round(t * 1e6, 2), "TFLOP/s": round(tfl, 1),
+                                 "frac_bf16_tensor": round(tfl / peaks["bf16_tflops"], 4),
+                                 "active_rows": active_rows,
+                                 "l2": "weights 264 MB > L2"}
 
 
 # -------------------------------------------------------------- CPU oracle --

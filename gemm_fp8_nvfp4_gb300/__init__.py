@@ -11,7 +11,8 @@ the calls raise.
 
 Entry points (same names as the C ABI without the ``gq_`` prefix):
 ``fp8_gemv``, ``nvfp4_gemv``, ``fp8_matmul``, ``nvfp4_matmul``,
-``fp8_grouped_matmul``, ``fp8_materialize``, ``nvfp4_materialize``.  The
+``fp8_grouped_matmul``, ``nvfp4_grouped_matmul``, ``fp8_materialize``,
+``nvfp4_materialize``.  The
 product calls take ``bias=`` and ``activation=`` for the fused epilogue
 (``out = act(alpha * acc + bias)``); with either given they call the ``_ex``
 form of the C entry point.  Outputs may be float32, bfloat16 or float16.
@@ -55,6 +56,10 @@ SIGNATURES = {
     "gq_nvfp4_matmul_ex": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _F, _E, _P]),
     "gq_fp8_grouped_matmul_ex": (_I, [_P, _I, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                       _I64, _I64, _E, _P]),
+    "gq_nvfp4_grouped_matmul": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                     _I64, _I64, _P]),
+    "gq_nvfp4_grouped_matmul_ex": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                        _I64, _I64, _I64, _E, _P]),
     "gq_fp8_materialize": (_I, [_P, _I, _P, _I64, _I64, _P]),
     "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
@@ -303,6 +308,46 @@ def fp8_grouped_matmul(a, w, a_offsets, expert_ids, expert_scales=None, max_rows
     return c
 
 
+def nvfp4_grouped_matmul(a, q, bs, a_offsets, expert_ids, expert_scales=None,
+                         max_rows_per_group=None, out=None, out_dtype=torch.bfloat16, stream=None,
+                         bias=None, activation="none"):
+    """Grouped MoE product with NVFP4 experts.  a [total_M, K] bf16,
+    q [E, N, K/2] uint8, bs [E, N, K/16] uint8 (e4m3 codes), a_offsets [G+1]
+    uint32/int32 (device), expert_ids [G] int32 (device), expert_scales [E]
+    float32 (the experts' second scales) or None, bias [E, N] or None."""
+    q, qp = _u8(q, "q", 3)
+    bs, bp = _u8(bs, "bs", 3)
+    ap = _dev(a, "a", torch.bfloat16, 2)
+    total_m, k = a.shape
+    e, n, half = q.shape
+    if half * 2 != k or tuple(bs.shape) != (e, n, k // 16):
+        raise ValueError("shapes must be a [M, K], q [E, N, K/2], bs [E, N, K/16]")
+    if a_offsets.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("a_offsets must be int32 or uint32")
+    op = _dev(a_offsets, "a_offsets", None, 1)
+    ip = _dev(expert_ids, "expert_ids", torch.int32, 1)
+    g = expert_ids.numel()
+    if a_offsets.numel() != g + 1:
+        raise ValueError("a_offsets must have G + 1 entries")
+    sp = None if expert_scales is None else _dev(expert_scales, "expert_scales", torch.float32, 1)
+    if max_rows_per_group is None:
+        max_rows_per_group = total_m
+    dtype = out.dtype if out is not None else out_dtype
+    c = _out(out, (total_m, n), dtype, a.device)
+    ep = _epilogue(bias, activation, (e, n))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_nvfp4_grouped_matmul(_dev(c, "out"), _out_code(dtype), ap, qp, bp, op, ip, sp,
+                                         g, e, int(max_rows_per_group), total_m, n, k,
+                                         _stream_handle(stream))
+    else:
+        st = lib.gq_nvfp4_grouped_matmul_ex(_dev(c, "out"), _out_code(dtype), ap, qp, bp, op, ip,
+                                            sp, g, e, int(max_rows_per_group), total_m, n, k,
+                                            _ref(ep), _stream_handle(stream))
+    _check(st, "nvfp4_grouped_matmul")
+    return c
+
+
 def fp8_materialize(w, out=None, out_dtype=torch.bfloat16, stream=None):
     """Dense e4m3(w) [N, K] as float32, bf16 or float16 (exact, unscaled)."""
     w, wp = _u8(w, "w", 2)
@@ -347,6 +392,7 @@ def device_status(reset: bool = False) -> int:
 
 __all__ = [
     "fp8_gemv", "nvfp4_gemv", "fp8_matmul", "nvfp4_matmul", "fp8_grouped_matmul",
+    "nvfp4_grouped_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
     "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
     "SIGNATURES", "LIB_PATH", "version", "status_str", "ACTIVATIONS", "Epilogue",

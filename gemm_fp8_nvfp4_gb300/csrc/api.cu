@@ -277,6 +277,44 @@ int gq_fp8_grouped_matmul(void* c_out, int out_dtype, const void* a, const uint8
                                   E, max_rows_per_group, total_M, N, K, nullptr, stream);
 }
 
+int gq_nvfp4_grouped_matmul_ex(void* c_out, int out_dtype, const void* a, const uint8_t* q,
+                               const uint8_t* bs, const uint32_t* a_offsets,
+                               const int32_t* expert_ids, const float* expert_scales, int64_t G,
+                               int64_t E, int64_t max_rows_per_group, int64_t total_M, int64_t N,
+                               int64_t K, const gq_epilogue* epilogue, cudaStream_t stream) {
+  if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
+  if (G < 0 || E < 0 || max_rows_per_group < 0 || total_M < 0 || N < 0 || K < 0 ||
+      K % 64 != 0)
+    return GQ_ERR_SHAPE;
+  if (K == 0 && epilogue != nullptr && epilogue->bias != nullptr) return GQ_ERR_SHAPE;
+  if (G == 0 || total_M == 0 || N == 0 || max_rows_per_group == 0) return GQ_OK;
+  if (!c_out || !a_offsets || !expert_ids || (K > 0 && (!a || (E > 0 && (!q || !bs)))))
+    return GQ_ERR_NULL;
+  if (!aligned(a, 16) || !aligned(q, 16) || !aligned(bs, 4) || !aligned(c_out, 16) ||
+      !aligned(a_offsets, 4) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4))
+    return GQ_ERR_ALIGN;
+  if (G > 65535 || E > 0x7FFFFFFFLL || total_M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL ||
+      K > 0x7FFFFFFFLL)
+    return GQ_ERR_TOO_LARGE;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, N, &ep)) return s;
+  gq::Ctx c;
+  if (int s = gq::device_ctx(stream, &c)) return s;
+  return gq::launch_status(gq::launch_nvfp4_grouped_gemm(c, c_out, ep, a, q, bs, a_offsets,
+                                                         expert_ids, expert_scales, G, E,
+                                                         max_rows_per_group, total_M, N, K));
+}
+
+int gq_nvfp4_grouped_matmul(void* c_out, int out_dtype, const void* a, const uint8_t* q,
+                            const uint8_t* bs, const uint32_t* a_offsets, const int32_t* expert_ids,
+                            const float* expert_scales, int64_t G, int64_t E,
+                            int64_t max_rows_per_group, int64_t total_M, int64_t N, int64_t K,
+                            cudaStream_t stream) {
+  return gq_nvfp4_grouped_matmul_ex(c_out, out_dtype, a, q, bs, a_offsets, expert_ids,
+                                    expert_scales, G, E, max_rows_per_group, total_M, N, K,
+                                    nullptr, stream);
+}
+
 int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w, int64_t N, int64_t K,
                        cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;

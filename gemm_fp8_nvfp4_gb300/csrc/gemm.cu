@@ -277,12 +277,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // (grouped: every expert's weight streams from DRAM once).
     auto prefetch_w = [&](const Tile& pt, int pkb) {
       if (lane != 0 || !pt.valid || pt.expert < 0) return;
-      if constexpr (F == Fmt::kFp8) {
-        if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * BK, pt.n0, pt.expert);
-        else tc::tma_prefetch_l2_2d(&tmap_w, pkb * BK, pt.n0);
-      } else {
-        tc::tma_prefetch_l2_2d(&tmap_w, pkb * (BK / 2), pt.n0);
-      }
+      constexpr int kBpk = (F == Fmt::kFp8) ? BK : BK / 2;   // weight bytes per row per K step
+      if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * kBpk, pt.n0, pt.expert);
+      else tc::tma_prefetch_l2_2d(&tmap_w, pkb * kBpk, pt.n0);
     };
     if (t_first < total_tiles) {
       const Tile first = get_tile<kGrouped>(p, t_first);
@@ -307,26 +304,22 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(&full_raw[s], kABytes + RawLayout<F>::kWBytes);
           tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0);
-          if constexpr (F == Fmt::kFp8) {
-            if constexpr (kGrouped) {
-              tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * BK, tl.n0, tl.expert);
-            } else {
-              tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * BK, tl.n0);
-            }
-          } else {
-            tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * (BK / 2), tl.n0);
-          }
+          constexpr int kBpk = (F == Fmt::kFp8) ? BK : BK / 2;
+          if constexpr (kGrouped) tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0, tl.expert);
+          else tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0);
         }
         if constexpr (F == Fmt::kNvfp4) {
-          // Block scales: 4 bytes (4 blocks of 16) per weight row per stage.
+          // Block scales: 4 bytes (4 blocks of 16) per weight row per stage;
+          // grouped: rows of expert e start at e * N.
           uint8_t* s_dst = smem + L::kSOff + s * RawLayout<F>::kScaleBytes;
           const int ks = p.K / 16;
+          const int64_t row_base = kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0;
 #pragma unroll
           for (int i = 0; i < BN / 32; ++i) {
             const int r = lane + 32 * i;
             const int n = tl.n0 + r;
             const bool in = n < p.N;
-            const uint8_t* src = scales_g + (static_cast<int64_t>(in ? n : 0) * ks + kb * 4);
+            const uint8_t* src = scales_g + ((row_base + (in ? n : 0)) * ks + kb * 4);
             tc::cp_async_4(s_dst + r * 4, src, in ? 4u : 0u);
           }
           tc::cp_async_mbar_arrive_noinc(&full_raw[s]);
@@ -717,6 +710,26 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void
   return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid);
 }
 
+// The grouped problem shared by both formats, and its persistent grid: an
+// upper bound of the work list (the exact count needs the device offsets),
+// capped at one CTA per SM.
+static Problem grouped_problem(const Ctx& c, void* out, const Epi& ep, const uint32_t* a_offsets,
+                               const int32_t* expert_ids, const float* expert_scales, int64_t G,
+                               int64_t E, int64_t max_rows, int64_t total_M, int64_t N, int64_t K,
+                               int* grid) {
+  Problem p = base_problem(c, out, ep, total_M, N, K, 1.0f);
+  p.a_offsets = a_offsets;
+  p.expert_ids = expert_ids;
+  p.expert_scales = expert_scales;
+  p.G = static_cast<int>(G);
+  p.E = (K > 0) ? static_cast<int>(E) : 0;
+  p.max_rows = static_cast<int>(std::min<int64_t>(max_rows, total_M));
+  const int64_t mt = (p.max_rows + BM - 1) / BM;
+  const int64_t bound = std::min<int64_t>(G * mt * p.num_n_tiles, 1LL << 30);
+  *grid = std::max(1, static_cast<int>(std::min<int64_t>(bound, c.num_sms)));
+  return p;
+}
+
 cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                                     const uint8_t* w, const uint32_t* a_offsets,
                                     const int32_t* expert_ids, const float* expert_scales,
@@ -734,18 +747,32 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep, cons
         !encode_3d(&tw, w, K, N, E, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
-  Problem p = base_problem(c, out, ep, total_M, N, K, 1.0f);
-  p.a_offsets = a_offsets;
-  p.expert_ids = expert_ids;
-  p.expert_scales = expert_scales;
-  p.G = static_cast<int>(G);
-  p.E = (K > 0) ? static_cast<int>(E) : 0;
-  p.max_rows = static_cast<int>(std::min<int64_t>(max_rows, total_M));
-  // Upper bound of the work list (the exact count needs the device offsets).
-  const int64_t mt = (p.max_rows + BM - 1) / BM;
-  const int64_t bound = std::min<int64_t>(G * mt * p.num_n_tiles, 1LL << 30);
-  const int grid = static_cast<int>(std::min<int64_t>(bound, c.num_sms));
-  return launch<Fmt::kFp8, true>(c, ta, tw, nullptr, p, grid > 0 ? grid : 1);
+  int grid = 1;
+  const Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
+                                    max_rows, total_M, N, K, &grid);
+  return launch<Fmt::kFp8, true>(c, ta, tw, nullptr, p, grid);
+}
+
+cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
+                                      const uint8_t* q, const uint8_t* bs, const uint32_t* a_offsets,
+                                      const int32_t* expert_ids, const float* expert_scales,
+                                      int64_t G, int64_t E, int64_t max_rows, int64_t total_M,
+                                      int64_t N, int64_t K) {
+  // As launch_fp8_grouped_gemm, with the packed expert stack q [E, N, K/2]
+  // (3-D tensor map, 32-byte swizzle) and block scales bs [E, N, K/16].
+  CUtensorMap ta, tw;
+  memset(&ta, 0, sizeof(ta));
+  memset(&tw, 0, sizeof(tw));
+  if (E > 0 && K > 0) {
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, total_M, K * 2, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&tw, q, K / 2, N, E, BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_32B))
+      return cudaErrorInvalidValue;
+  }
+  int grid = 1;
+  const Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
+                                    max_rows, total_M, N, K, &grid);
+  return launch<Fmt::kNvfp4, true>(c, ta, tw, bs, p, grid);
 }
 
 }  // namespace gq

@@ -80,6 +80,14 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                     int64_t E, int64_t max_rows,
                                     int64_t total_M, int64_t N, int64_t K);
 
+cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
+                                      const void* a, const uint8_t* q,
+                                      const uint8_t* bs, const uint32_t* a_offsets,
+                                      const int32_t* expert_ids,
+                                      const float* expert_scales, int64_t G,
+                                      int64_t E, int64_t max_rows,
+                                      int64_t total_M, int64_t N, int64_t K);
+
 // gemm_skinny.cu (M <= skinny_max_rows())
 int skinny_max_rows();
 bool nvfp4_skinny_ok(const uint8_t* bs, int64_t K);   // the NVFP4 few-row kernel takes this K

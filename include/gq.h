@@ -232,6 +232,34 @@ int gq_fp8_grouped_matmul_ex(void* c, int out_dtype, const void* a,
                              const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
+ * Grouped (MoE) NVFP4 GEMM: gq_fp8_grouped_matmul's groups with NVFP4 experts.
+ * Source: the "Matmul2dFp8" page, method run_grouped (the grouped schedule),
+ * and the "fp4_matmul" page (the NVFP4 weight): for every group z, rows
+ * r in [a_offsets[z], a_offsets[z+1]):
+ *     c[r, :] = 0                                              if expert_ids[z] == -1
+ *     c[r, :] = s_e * a[r, :] @ (e2m1(q[e]) * e4m3(bs[e]))^T   with e = expert_ids[z],
+ *               s_e = expert_scales[e] (the expert's second scale; 1 when NULL)
+ *   c [total_M, N] (out_dtype), a [total_M, K] bfloat16,
+ *   q [E, N, K/2] uint8 (packed, low nibble first), bs [E, N, K/16] uint8,
+ *   a_offsets, expert_ids, expert_scales, max_rows_per_group: as in
+ *   gq_fp8_grouped_matmul (same defensive treatment of device-side data).
+ * K % 64 == 0.  Pointers 16-byte aligned, bs 4-byte.
+ */
+int gq_nvfp4_grouped_matmul(void* c, int out_dtype, const void* a, const uint8_t* q,
+                            const uint8_t* bs, const uint32_t* a_offsets,
+                            const int32_t* expert_ids, const float* expert_scales,
+                            int64_t G, int64_t E, int64_t max_rows_per_group,
+                            int64_t total_M, int64_t N, int64_t K, cudaStream_t stream);
+/* The same with a fused epilogue; its bias is [E, N].  K = 0 with a bias
+ * returns GQ_ERR_SHAPE.  NULL = gq_nvfp4_grouped_matmul. */
+int gq_nvfp4_grouped_matmul_ex(void* c, int out_dtype, const void* a, const uint8_t* q,
+                               const uint8_t* bs, const uint32_t* a_offsets,
+                               const int32_t* expert_ids, const float* expert_scales,
+                               int64_t G, int64_t E, int64_t max_rows_per_group,
+                               int64_t total_M, int64_t N, int64_t K,
+                               const gq_epilogue* epilogue, cudaStream_t stream);
+
+/*
  * FP8 materialize: out[n, k] = e4m3(w[n, k]) as float32, bfloat16 or binary16,
  * exact (every E4M3 value is representable in all three), no scale applied.
  * Source: "fp8_gemv" page -- enqueue_fp8_materialize / fp8_materialize_kernel.

@@ -112,6 +112,17 @@ def nvfp4_weight(n: int, k: int, seed: int = 0, device="cpu"):
     return q.to(device), bs.contiguous().to(device), scale2
 
 
+def nvfp4_expert_stack(e: int, n: int, k: int, seed: int = 0, device="cpu"):
+    """(q uint8 [e, n, k/2], bs uint8 [e, n, k/16], scale2 float32 [e]): one
+    NVFP4 weight per expert, expert j drawn with seed * 1000 + j."""
+    q = torch.empty((e, n, k // 2), dtype=torch.uint8)
+    bs = torch.empty((e, n, k // 16), dtype=torch.uint8)
+    s2 = torch.empty(e, dtype=torch.float32)
+    for j in range(e):
+        q[j], bs[j], s2[j] = nvfp4_weight(n, k, seed * 1000 + j)
+    return q.to(device), bs.to(device), s2.to(device)
+
+
 def moe_routing(total_rows: int, seed: int = 2):
     """(a_offsets int64 [G+1], expert_ids int64 [G], counts [G]) for the
     9-category routing described in the module docstring."""
