@@ -198,11 +198,13 @@ int gq_fp8_matmul_ex(void* c_out, int out_dtype, const void* a, const uint8_t* w
                      int64_t N, int64_t K, float alpha, const gq_epilogue* epilogue,
                      cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
-  if (M < 0 || N < 0 || K < 0 || K % 16 != 0) return GQ_ERR_SHAPE;
+  if (M < 0 || N < 0 || K < 0) return GQ_ERR_SHAPE;
   if (M == 0 || N == 0) return GQ_OK;
   if (!c_out || (K > 0 && (!a || !w))) return GQ_ERR_NULL;
   if (!aligned(a, 16) || !aligned(w, 16) || !aligned(c_out, 16)) return GQ_ERR_ALIGN;
   if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  // K not a multiple of 16: the tensor-map coordinates reach 16 K (int32).
+  if (K % 16 != 0 && K > (1LL << 27)) return GQ_ERR_TOO_LARGE;
   gq::Epi ep;
   if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;

@@ -34,12 +34,25 @@
 //                 scale, convert (RNE) and store with bounds guards.
 // Tiles are visited m-fastest so that consecutive CTAs share a weight tile
 // through L2 (the pages' Morton raster serves the same purpose).
+//
+// Any K (FP8 only; the "fp4_matmul" page's K-strip plus tail loop): when K is
+// not a multiple of 16 the rows of A (2K bytes) and W (K bytes) are not
+// 16-byte strided, but rows 8 apart in A and 16 apart in W are (16K bytes).
+// So A is described as [M/8 groups, 8K elements] and W as [N/16 groups, 16K
+// bytes]: one TMA box per residue class (row mod 8, row mod 16) brings the
+// 16-byte-aligned windows around the stage's K range of every row of that
+// class (rows of an incomplete last group come by cp.async).  The dequant
+// warps then shift each row by its fixed misalignment, zero the K tail, and
+// write A and the decoded weight in the swizzled layout.  A's rows are
+// realigned in place and kept in residue order (tile row 8 i + r at smem row
+// 32 r + i), which the epilogue undoes when it picks the output row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemm_common.cuh"
@@ -83,6 +96,10 @@ template <> struct RawLayout<Fmt::kNvfp4> {
 };
 
 template <Fmt F> struct Smem {
+  static constexpr int kRawSt = kRawStages;     // A + raw weight ring
+  static constexpr int kDeqSt = kDeqStages;     // decoded weight ring
+  static constexpr uint32_t kAStride = kABytes;
+  static constexpr uint32_t kDeqStride = kDeqBytes;
   static constexpr uint32_t kDeqOff = 0;
   static constexpr uint32_t kAOff = kDeqOff + kDeqStages * kDeqBytes;
   static constexpr uint32_t kWOff = kAOff + kRawStages * kABytes;
@@ -96,9 +113,47 @@ template <Fmt F> struct Smem {
   static constexpr uint32_t kAlloc = kTotal + 1024;              // slack for 1 KB alignment
 };
 
+// Any-K layout: two stages, each [A 32 KB | decoded W 32 KB | A side rows |
+// raw W boxes | cp.async rows].  The A box of residue r (rows 8 i + r,
+// i < 28; 144 bytes each) lands inside the 4 KB of smem rows 32 r .. 32 r + 31,
+// which the same warp overwrites with the realigned rows after reading them;
+// the box for i = 28..31 lands in the side area.
+constexpr uint32_t kAnyRowA = 144;                 // raw A window bytes per row
+constexpr uint32_t kAnyRowW = 80;                  // raw weight window bytes per row
+constexpr int kAnyInTile = 28;                     // A box rows that land in place
+constexpr uint32_t kAnySideSlot = 640;             // 4 x 144 bytes, rounded to 128
+constexpr uint32_t kAnyWBox = 16 * kAnyRowW;       // 1280: W box of one residue
+static_assert(kAnyInTile * kAnyRowA <= 32 * BK * 2, "in-place A rows fit their 4 KB");
+struct SmemAnyK {
+  static constexpr int kRawSt = 2;
+  static constexpr int kDeqSt = 2;
+  static constexpr uint32_t kAOff = 0;
+  static constexpr uint32_t kDeqOff = kABytes;
+  static constexpr uint32_t kSideOff = kABytes + kDeqBytes;
+  static constexpr uint32_t kWOff = kSideOff + 8 * kAnySideSlot;
+  static constexpr uint32_t kPartAOff = kWOff + 16 * kAnyWBox;       // <= 7 rows of A
+  static constexpr uint32_t kPartWOff = kPartAOff + 1024;             // <= 15 rows of W
+  static constexpr uint32_t kStage = (kPartWOff + 1280 + 1023) & ~1023u;
+  static constexpr uint32_t kAStride = kStage;
+  static constexpr uint32_t kDeqStride = kStage;
+  static constexpr uint32_t kBarOff = 2 * kStage;
+  static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kTotal = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kTotal + 1024;
+  // Transaction bytes of one stage's boxes.
+  static constexpr uint32_t kABoxBytes = 8 * 32 * kAnyRowA;
+  static constexpr uint32_t kWBoxBytes = 16 * kAnyWBox;
+};
+
+template <Fmt F, bool kAnyK>
+using SmemFor = typename std::conditional<kAnyK, SmemAnyK, Smem<F>>::type;
+
 static_assert(UMMA_M * kPartStride <= Smem<Fmt::kNvfp4>::kBarOff &&
-                  UMMA_M * kPartStride <= Smem<Fmt::kFp8>::kBarOff,
+                  UMMA_M * kPartStride <= Smem<Fmt::kFp8>::kBarOff &&
+                  UMMA_M * kPartStride <= SmemAnyK::kBarOff,
               "split-K partials fit below the barriers");
+static_assert(SmemAnyK::kAlloc <= 232448, "any-K stages fit in shared memory");
 
 // Work description shared by the plain and grouped GEMMs.
 struct Problem {
@@ -112,7 +167,10 @@ struct Problem {
   int num_n_tiles;
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
+  int a_groups, w_groups;      // any-K path: full 8-row groups of A, 16-row groups of W
   Epi ep;                      // output type and fused epilogue
+  const void* a_g;             // any-K path: A [M, K] bf16 (read with plain loads)
+  const uint8_t* w_g;          // any-K path: W [N, K] e4m3 codes
   int ksplit;                  // > 1: split-K over a thread-block cluster of ksplit CTAs
   int kb_per_split;            // K steps per split
 };
@@ -199,13 +257,63 @@ __device__ __forceinline__ int num_tiles(const Problem& p) {
   else return plain_num_tiles(p);
 }
 
+// ------------------------------------------------------ any-K loading --
+
+// Where the raw window of residue r, group index i (tile row 8 i + r) of a
+// stage lands, relative to the stage.
+__device__ __forceinline__ uint32_t any_raw_a_off(int r, int i) {
+  return i < kAnyInTile ? static_cast<uint32_t>(r * 4096 + i * kAnyRowA)
+                        : SmemAnyK::kSideOff + r * kAnySideSlot + (i - kAnyInTile) * kAnyRowA;
+}
+
+// The bytes [off, off + 4 N) of in[] (off = 0..15, a per-row constant), as
+// N words: a two-step word shift by off / 4 and a funnel shift by off % 4,
+// with constant register indices.
+template <int N>
+__device__ __forceinline__ void realign_words(const uint32_t (&in)[N + 4], uint32_t off,
+                                              uint32_t (&out)[N]) {
+  const bool s2 = off & 8, s1 = off & 4;
+  const uint32_t sh = (off & 3) * 8;
+  uint32_t t[N + 2], u[N + 1];
+#pragma unroll
+  for (int i = 0; i < N + 2; ++i) t[i] = s2 ? in[i + 2] : in[i];
+#pragma unroll
+  for (int i = 0; i < N + 1; ++i) u[i] = s1 ? t[i + 1] : t[i];
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(u[i], u[i + 1], sh);
+}
+
+// Zero the bytes at or after nbytes (the K tail of the last stage).
+template <int N>
+__device__ __forceinline__ void mask_tail(uint32_t (&w)[N], int nbytes) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int rem = nbytes - 4 * i;
+    const uint32_t m = rem >= 4 ? 0xFFFFFFFFu : rem <= 0 ? 0u : (1u << (8 * rem)) - 1u;
+    w[i] &= m;
+  }
+}
+
+// Prefetch the bytes [lo, hi) of a buffer that starts 16-byte aligned at
+// `base` into L2, in 32 KB pieces spread over the lanes of a warp; the range
+// is shrunk to 16-byte boundaries inside [base, hi).
+__device__ __forceinline__ void prefetch_span_l2(const uint8_t* base, int64_t lo, int64_t hi,
+                                                 int lane) {
+  lo &= ~static_cast<int64_t>(15);
+  hi &= ~static_cast<int64_t>(15);
+  constexpr int64_t kPiece = 32768;
+  for (int64_t o = lo + lane * kPiece; o < hi; o += 32 * kPiece)
+    tc::bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(kPiece, hi - o)));
+}
+
 // ----------------------------------------------------------------- kernel --
 
-template <Fmt F, bool kGrouped>
+template <Fmt F, bool kGrouped, bool kAnyK>
 __global__ void __launch_bounds__(kThreads, 1)
 k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-          const uint8_t* __restrict__ scales_g, Problem p) {
-  using L = Smem<F>;
+          const __grid_constant__ CUtensorMap tmap_x, const uint8_t* __restrict__ scales_g,
+          Problem p) {
+  using L = SmemFor<F, kAnyK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -225,10 +333,14 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const uint32_t smem_base = tc::smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    constexpr uint32_t kRawArrivals = (F == Fmt::kNvfp4) ? 1 + 32 : 1;
+    // The raw stage is full after the copies (+ the NVFP4 scale copies).  It
+    // is empty after the MMA (+ the dequant warps that read its raw weight;
+    // any K: the loader warps finish with a stage before the MMA starts).
+    constexpr uint32_t kRawArrivals = (kAnyK || F == Fmt::kNvfp4) ? 1 + 32 : 1;
+    constexpr uint32_t kRawReleases = kAnyK ? 1 : 1 + kDeqWarps;
     for (int s = 0; s < kRawStages; ++s) {
       tc::mbar_init(&full_raw[s], kRawArrivals);
-      tc::mbar_init(&empty_raw[s], 1 + kDeqWarps);
+      tc::mbar_init(&empty_raw[s], kRawReleases);
     }
     for (int s = 0; s < kDeqStages; ++s) {
       tc::mbar_init(&full_deq[s], kDeqWarps);
@@ -246,9 +358,16 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
-  if (warp == kWarpTma && lane == 0 && p.num_k_blocks > 0 && (!kGrouped || p.E > 0)) {
+  if (!kAnyK && warp == kWarpTma && lane == 0 && p.num_k_blocks > 0 && (!kGrouped || p.E > 0)) {
     tc::tma_prefetch_desc(&tmap_a);
     tc::tma_prefetch_desc(&tmap_w);
+  }
+  if (kAnyK && warp == kWarpTma && lane == 0) {
+    if (p.a_groups > 0) {
+      tc::tma_prefetch_desc(&tmap_a);
+      tc::tma_prefetch_desc(&tmap_x);
+    }
+    if (p.w_groups > 0) tc::tma_prefetch_desc(&tmap_w);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -266,7 +385,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
 
-  if (warp == kWarpTma) {
+  if (warp == kWarpTma && !kAnyK) {
     // ------------------------------------------------------ TMA producer --
     int s = 0;
     uint32_t ph = 0;
@@ -337,6 +456,106 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
       }
     }
+  } else if (kAnyK && warp == kWarpTma) {
+    // ------------------------------------------------ any-K TMA producer --
+    // Lane 0: per stage 8 + 8 A boxes (residue r: rows 8 i + r, i < 28 and
+    // i >= 28) and 16 W boxes (residue r: rows 16 i + r), each starting at the
+    // stage's K offset of its residue rounded down to 16 bytes.  All lanes:
+    // the rows past the last full group by 16-byte cp.async (a chunk that
+    // crosses the end of its buffer copies only the bytes inside it).
+    const uint8_t* a_g = static_cast<const uint8_t*>(p.a_g);
+    const int64_t K = p.K;
+    const uint8_t* a_end = a_g + 2 * static_cast<int64_t>(p.M) * K;
+    const uint8_t* w_end = p.w_g + static_cast<int64_t>(p.N) * K;
+    const int a_full = 8 * p.a_groups;             // rows covered by the A maps
+    const int w_full = 16 * p.w_groups;            // rows covered by the W map
+    auto prefetch_tile = [&](int pt_i) {
+      if (pt_i >= total_tiles) return;
+      const Tile pt = get_tile<kGrouped>(p, pt_i);
+      if (!pt.valid || pt.expert < 0) return;
+      prefetch_span_l2(p.w_g, pt.n0 * K + kb0 * BK, static_cast<int64_t>(min(pt.n0 + BN, p.N)) * K, lane);
+      prefetch_span_l2(a_g, 2 * (pt.m0 * K + kb0 * BK), 2 * static_cast<int64_t>(pt.m_end) * K, lane);
+    };
+    // One 16-byte chunk at the 16-byte-aligned address src; `any` is a valid
+    // address passed when no byte is read.
+    auto copy_chunk = [&](uint8_t* dst, const uint8_t* src, const uint8_t* end, const uint8_t* any) {
+      const int64_t left = end - src;
+      const uint32_t n = left >= 16 ? 16u : left > 0 ? static_cast<uint32_t>(left) : 0u;
+      tc::cp_async_16(dst, n ? src : any, n);
+    };
+    constexpr uint32_t kTx0 = SmemAnyK::kABoxBytes, kTx1 = SmemAnyK::kWBoxBytes;
+    const uint32_t tx = (p.a_groups > 0 ? kTx0 : 0u) + (p.w_groups > 0 ? kTx1 : 0u);
+    prefetch_tile(t_first);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = t_first; t < total_tiles && ok; t += t_step) {
+      const Tile tl = get_tile<kGrouped>(p, t);
+      prefetch_tile(t + t_step);
+      if (!tl.valid || tl.expert < 0) continue;
+      const bool a_part = tl.m_end > a_full;
+      const bool w_part = min(tl.n0 + BN, p.N) > w_full;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        const int64_t k0 = static_cast<int64_t>(kb) * BK;
+        uint8_t* st = smem + s * SmemAnyK::kStage;
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(&full_raw[s], tx);
+          if (p.a_groups > 0) {
+            const int g0 = tl.m0 / 8;
+#pragma unroll 1
+            for (int r = 0; r < 8; ++r) {
+              const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(7));
+              tc::tma_load_2d(st + any_raw_a_off(r, 0), &tmap_a, &full_raw[s], x0, g0);
+              tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile), &tmap_x, &full_raw[s], x0,
+                              g0 + kAnyInTile);
+            }
+          }
+          if (p.w_groups > 0) {
+            const int g0 = tl.n0 / 16;
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+              const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(15));
+              tc::tma_load_2d(st + SmemAnyK::kWOff + r * kAnyWBox, &tmap_w, &full_raw[s], x0, g0);
+            }
+          }
+        }
+        if (a_part) {
+          for (int c = lane; c < 7 * 9; c += 32) {
+            const int r = c / 9, j = c - 9 * r;
+            const int m = a_full + r;
+            if (m < tl.m0 || m >= tl.m_end) continue;
+            const uintptr_t w0 = reinterpret_cast<uintptr_t>(a_g + 2 * (m * K + k0)) & ~static_cast<uintptr_t>(15);
+            copy_chunk(st + SmemAnyK::kPartAOff + r * kAnyRowA + 16 * j,
+                       reinterpret_cast<const uint8_t*>(w0) + 16 * j, a_end, a_g);
+          }
+        }
+        if (w_part) {
+          for (int c = lane; c < 15 * 5; c += 32) {
+            const int r = c / 5, j = c - 5 * r;
+            const int n = w_full + r;
+            if (n < tl.n0 || n >= p.N || n >= tl.n0 + BN) continue;
+            const uintptr_t w0 = reinterpret_cast<uintptr_t>(p.w_g + n * K + k0) & ~static_cast<uintptr_t>(15);
+            copy_chunk(st + SmemAnyK::kPartWOff + r * kAnyRowW + 16 * j,
+                       reinterpret_cast<const uint8_t*>(w0) + 16 * j, w_end, p.w_g);
+          }
+        }
+        tc::cp_async_mbar_arrive_noinc(&full_raw[s]);
+        if (++s == SmemAnyK::kRawSt) { s = 0; ph ^= 1; }
+      }
+    }
+    // Drain: no copy may still land when the CTA exits.
+    if (lane == 0) {
+      int ds = s;
+      uint32_t dph = ph;
+      for (int i = 0; i < SmemAnyK::kRawSt; ++i) {
+        if (--ds < 0) { ds = SmemAnyK::kRawSt - 1; dph ^= 1; }
+        tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
+      }
+    }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
     constexpr uint32_t kIdesc = tc::idesc_bf16_f32(UMMA_M, BN);
@@ -349,7 +568,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       if (!tl.valid || tl.expert < 0) continue;
       const uint32_t acc_ph = it & 1;
       ++it;
-      const bool two_halves = tl.m_end - tl.m0 > UMMA_M;
+      // (Any K: the rows are in residue order, spread over both halves.)
+      const bool two_halves = kAnyK || tl.m_end - tl.m0 > UMMA_M;
       // Both accumulators free (the epilogue of the previous tile has read them).
       if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
@@ -361,8 +581,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         tc::tc_fence_after();
         if (lane == 0) {
-          const uint32_t a_addr = smem_base + L::kAOff + s * kABytes;
-          const uint32_t b_addr = smem_base + L::kDeqOff + d * kDeqBytes;
+          const uint32_t a_addr = smem_base + L::kAOff + s * L::kAStride;
+          const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
@@ -378,8 +598,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           tc::mma_commit(&empty_deq[d]);
         }
         __syncwarp();
-        if (++s == kRawStages) { s = 0; ph ^= 1; }
-        if (++d == kDeqStages) { d = 0; dph ^= 1; }
+        if (++s == L::kRawSt) { s = 0; ph ^= 1; }
+        if (++d == L::kDeqSt) { d = 0; dph ^= 1; }
       }
       if (!ok) break;
       if (lane == 0) tc::mma_commit(&tmem_full[0]);
@@ -391,7 +611,102 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       tc::mbar_wait_quiet(drain, 0, 100000000ull);
     }
     __syncwarp();
-  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+  } else if (kAnyK && warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+    // ----------------------------------------- any-K realign + dequant --
+    // Thread t owns smem A row t (residue t / 32, group index t % 32) and one
+    // weight row chosen so that the 8 threads of each quarter warp read
+    // distinct 16-byte bank groups of the raw boxes and write distinct ones of
+    // the swizzled tile: residue u + 8 (g & 1), group index (u + g / 2) mod 16
+    // for t = 8 g + u.  Each raw window is shifted by its fixed misalignment,
+    // the K tail of the last stage is zeroed, and rows past the end are zero.
+    const int t = threadIdx.x - kDeqWarp0 * 32;
+    const int ar = t >> 5, ai = t & 31;               // A residue, group index
+    const int wr = (t & 7) + 8 * ((t >> 3) & 1);      // W residue
+    const int wi = ((t & 7) + (t >> 4)) & 15;         // W group index
+    const int wrow = 16 * wi + wr;                    // W tile row
+    const int64_t K = p.K;
+    const int a_full = 8 * p.a_groups;
+    const int w_full = 16 * p.w_groups;
+    const uint32_t off_a = static_cast<uint32_t>((2 * ar * K) & 15);
+    const uint32_t off_w = static_cast<uint32_t>((wr * K) & 15);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tt = t_first; tt < total_tiles && ok; tt += t_step) {
+      const Tile tl = get_tile<kGrouped>(p, tt);
+      if (!tl.valid || tl.expert < 0) continue;
+      const int m = tl.m0 + 8 * ai + ar;
+      const bool a_act = m < tl.m_end;
+      const uint32_t a_src = m < a_full ? any_raw_a_off(ar, ai)
+                                        : SmemAnyK::kPartAOff + (m - a_full) * kAnyRowA;
+      const int n = tl.n0 + wrow;
+      const bool w_act = n < p.N;
+      const uint32_t w_src = n < w_full ? SmemAnyK::kWOff + wr * kAnyWBox + wi * kAnyRowW
+                                        : SmemAnyK::kPartWOff + (n - w_full) * kAnyRowW;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant)) {
+          ok = false;
+          break;
+        }
+        const int kv = min(BK, p.K - kb * BK);     // valid K of this stage, >= 1
+        const uint32_t st = smem_base + s * SmemAnyK::kStage;
+        {
+          uint32_t out[32];
+          if (a_act) {
+            uint32_t in[36];
+#pragma unroll
+            for (int c = 0; c < 9; ++c) {
+              const uint4 v = tc::lds128(st + a_src + 16 * c);
+              in[4 * c] = v.x; in[4 * c + 1] = v.y; in[4 * c + 2] = v.z; in[4 * c + 3] = v.w;
+            }
+            realign_words<32>(in, off_a, out);
+            if (kv < BK) mask_tail<32>(out, 2 * kv);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) out[i] = 0u;
+          }
+          __syncwarp();                             // every raw row of the warp is read
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            tc::sts128(st + sw128_off(t, c),
+                       make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]));
+        }
+        {
+          constexpr uint16_t kOne = 0x3C00;         // 1.0 in f16
+          uint32_t code[16];
+          if (w_act) {
+            uint32_t in[20];
+#pragma unroll
+            for (int c = 0; c < 5; ++c) {
+              const uint4 v = tc::lds128(st + w_src + 16 * c);
+              in[4 * c] = v.x; in[4 * c + 1] = v.y; in[4 * c + 2] = v.z; in[4 * c + 3] = v.w;
+            }
+            realign_words<16>(in, off_w, code);
+            if (kv < BK) mask_tail<16>(code, kv);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) code[i] = 0u;
+          }
+          const uint32_t dst = st + SmemAnyK::kDeqOff;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t h0, h1, h2, h3;
+            e4m3x4_to_h2x2(code[2 * c], h0, h1);
+            e4m3x4_to_h2x2(code[2 * c + 1], h2, h3);
+            tc::sts128(dst + sw128_off(wrow, c),
+                       make_uint4(f32x2_hi_to_bf16x2(h2_scale_f32(h0, kOne)),
+                                  f32x2_hi_to_bf16x2(h2_scale_f32(h1, kOne)),
+                                  f32x2_hi_to_bf16x2(h2_scale_f32(h2, kOne)),
+                                  f32x2_hi_to_bf16x2(h2_scale_f32(h3, kOne))));
+          }
+        }
+        tc::fence_proxy_async_smem();   // make the generic stores visible to the tensor core
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&full_deq[s]);
+        if (++s == SmemAnyK::kRawSt) { s = 0; ph ^= 1; }
+      }
+    }
+  } else if (!kAnyK && warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ---------------------------------------------------------- dequant --
     const int row = threadIdx.x - kDeqWarp0 * 32;  // 0..255: weight row in the tile
     int s = 0, d = 0;
@@ -504,10 +819,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const bool plain_epi = epi_plain(p.ep);
       const bool vec_ok = p.ep.out_kind == kOutF32 ? (p.N % 4 == 0) : (p.N % 8 == 0);
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
-      const int halves = tl.m_end - tl.m0 > UMMA_M ? 2 : 1;
+      const int halves = (kAnyK || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
-        const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
+        // TMEM lane h * 128 + 32 g + lane holds tile row h * 128 + 32 g + lane,
+        // or (any K, residue order) tile row 8 lane + 4 h + g.
+        const int m = kAnyK ? tl.m0 + 8 * lane + 4 * h + g : tl.m0 + h * UMMA_M + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
 #pragma unroll 1
@@ -606,11 +923,11 @@ __global__ void k_fill_scaled_zero(void* out, Epi ep, int64_t count, int64_t N, 
 
 // --------------------------------------------------------------- host --
 
-template <Fmt F, bool kGrouped>
+template <Fmt F, bool kGrouped, bool kAnyK = false>
 cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, const uint8_t* scales,
-                   const Problem& p, int grid) {
-  auto kern = k_wq_gemm<F, kGrouped>;
-  const uint32_t smem = Smem<F>::kAlloc;
+                   const Problem& p, int grid, const CUtensorMap* tx = nullptr) {
+  auto kern = k_wq_gemm<F, kGrouped, kAnyK>;
+  const uint32_t smem = SmemFor<F, kAnyK>::kAlloc;
   // The shared-memory opt-in is set once per device (it is not a stream
   // operation, so it is kept out of any CUDA-graph capture after the first call).
   static std::atomic<uint64_t> configured{0};
@@ -632,7 +949,9 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.ksplit > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tw, scales, p);
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, scales, p);
 }
 
 cudaError_t fill_zero(const Ctx& c, void* out, const Epi& ep, int64_t count, int64_t N, float alpha) {
@@ -680,6 +999,31 @@ int plan_split(const Ctx& c, Problem& p, int tiles) {
 cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* a, const uint8_t* w,
                             int64_t M, int64_t N, int64_t K, float alpha) {
   if (K == 0) return fill_zero(c, out, ep, M * N, N, alpha);
+  if (K % 16 != 0) {
+    // Rows not 16-byte strided: rows 8 (A) and 16 (W) apart are.  Tensor maps
+    // over the full groups (any M, no split-K).
+    CUtensorMap ta, tx, tw;
+    memset(&ta, 0, sizeof(ta));
+    memset(&tx, 0, sizeof(tx));
+    memset(&tw, 0, sizeof(tw));
+    Problem p = base_problem(c, out, ep, M, N, K, alpha);
+    p.a_g = a;
+    p.w_g = w;
+    p.a_groups = static_cast<int>(M / 8);
+    p.w_groups = static_cast<int>(N / 16);
+    if (p.a_groups > 0 &&
+        (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72, kAnyInTile,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72,
+                    32 - kAnyInTile, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return cudaErrorInvalidValue;
+    if (p.w_groups > 0 &&
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 16 * K, N / 16, 16 * K, kAnyRowW, 16,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
+    return launch<Fmt::kFp8, false, true>(c, ta, tw, nullptr, p, std::min(tiles, c.num_sms), &tx);
+  }
   if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, ep, a, w, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,

@@ -127,6 +127,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // Prefetch a tensor tile into L2 (no shared-memory destination, no completion).
+// Untiled bulk prefetch into L2: addr 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
@@ -149,7 +154,8 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
                : "memory");
 }
 
-// 16-byte cp.async (L2 only) with zero fill: copies src_bytes (0 or 16).
+// 16-byte cp.async (L2 only) with zero fill: copies src_bytes (0..16) and
+// fills the rest of the 16 bytes with zeros.
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "r"(src_bytes)
@@ -332,6 +338,10 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t lo, uint32_t hi) {
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {

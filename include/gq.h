@@ -166,8 +166,12 @@ int gq_nvfp4_gemv_ex(void* y, int out_dtype, const void* x, const uint8_t* q,
  * Source: "fp8_gemv" page -- enqueue_apple_fp8_matmul (raw W8A16 matmul);
  * "Matmul2dFp8" page (bf16 A x fp8 B -> fp32, c_type output).
  *   c [M, N] (out_dtype), a [M, K] bfloat16, w [N, K] float8_e4m3fn.
- * K % 16 == 0 (GQ_ERR_SHAPE otherwise): the tensor-memory-accelerator row
- * stride rule.  M, N arbitrary.  Pointers 16-byte aligned.
+ * M, N, K arbitrary.  Pointers 16-byte aligned.  With K % 16 == 0 the
+ * operands are staged by the tensor memory accelerator; otherwise their rows
+ * are not 16-byte strided: they are staged by residue class (rows 8 apart in
+ * a, 16 apart in w are 16-byte strided) and realigned in shared memory (the
+ * "fp4_matmul" page's K tail, generalised to any K); then K <= 2^27
+ * (GQ_ERR_TOO_LARGE otherwise).
  */
 int gq_fp8_matmul(void* c, int out_dtype, const void* a, const uint8_t* w,
                   int64_t M, int64_t N, int64_t K, float alpha,

@@ -160,7 +160,7 @@ def test_gemm_errors():
     a = torch.zeros(4, 32, dtype=torch.bfloat16, device=DEV)
     w = torch.zeros(8, 32, dtype=torch.uint8, device=DEV)
     c = torch.zeros(4, 8, dtype=torch.float32, device=DEV)
-    assert l.gq_fp8_matmul(c.data_ptr(), 0, a.data_ptr(), w.data_ptr(), 4, 8, 24, 1.0, s) == 2
+    assert l.gq_fp8_matmul(c.data_ptr(), 0, a.data_ptr(), w.data_ptr(), 4, 8, -1, 1.0, s) == 2
     assert l.gq_fp8_matmul(c.data_ptr(), 0, a.data_ptr() + 2, w.data_ptr(), 4, 8, 32, 1.0, s) == 3
     assert l.gq_fp8_matmul(c.data_ptr(), 0, None, w.data_ptr(), 4, 8, 32, 1.0, s) == 1
     assert l.gq_nvfp4_matmul(c.data_ptr(), 0, a.data_ptr(), w.data_ptr(), w.data_ptr(), 4, 8, 32,
