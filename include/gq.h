@@ -32,7 +32,8 @@
  *     sum this equals folding the scale after the matmul.
  *   - Pointer alignment: 16 bytes for every tensor pointer (weights,
  *     activations, outputs); block scales need 1 byte.  Odd K is allowed for
- *     the FP8 GEMV (it picks a narrower load width); see each call.
+ *     the FP8 GEMV (it picks a narrower load width) and the FP8 GEMM (rows
+ *     staged by residue class); see each call.
  *   - Zero-sized M or N: nothing is queued, GQ_OK.  K = 0: outputs are written
  *     as alpha * 0 (through the epilogue, when there is one).
  *   - Results are deterministic: a given call on given inputs returns the same
