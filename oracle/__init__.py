@@ -16,14 +16,17 @@ with numpy:
   the grouped (MoE) form loops over groups and runs a dense product per group;
   materialize returns the decoded weight itself;
 * the optional fused epilogue (``epilogue``): bias add and an activation,
-  and the binary16 output rounding (``formats.f64_to_f16_bits``).
+  and the binary16 output rounding (``formats.f64_to_f16_bits``);
+* the W8A8 int8 sibling method (``w8a8``): per-row absmax activation
+  quantization, the exact int8 x int8 sum and its float32 dequant.
 
 Sources (Modular kernel API pages for Apple M5):
   * "fp8_gemv" module page: the W8A16 GEMV, the scale contract, materialize;
   * "fp4_matmul" module page: the packed NVFP4 weight layout and block scales;
   * "Matmul2dFp8" struct page, method ``run_grouped``: the grouped MoE product;
     its parameters c_type (fp16 / bf16 / fp32 output) and elementwise_lambda_fn
-    (the fused epilogue).
+    (the fused epilogue);
+  * "int8_matmul" module page: the W8A8 quantizer and product.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against what the
 pages and the formats fix (exhaustive code tables, closed forms, brute force in
@@ -34,6 +37,8 @@ example of the layer itself, so no function is pinned to a printed value.
 from .formats import (e4m3_table, e2m1_table, bf16_bits_to_f64, f64_to_bf16_bits,
                       f16_bits_to_f64, f64_to_f16_bits)
 from .decode import decode_fp8, decode_nvfp4, nibble
+from .w8a8 import (int8_quantize_rows, int8_accumulate, int8_dequant, int8_matmul,
+                   int8_abs_sum)
 from .layer import (
     linear,
     linear_loops,
@@ -63,4 +68,5 @@ __all__ = [
     "nvfp4_materialize", "abs_dot", "bf16_ulp", "tolerance",
     "f16_bits_to_f64", "f64_to_f16_bits", "f16_ulp", "activation", "ACT_LIPSCHITZ",
     "epilogue", "tolerance_epilogue",
+    "int8_quantize_rows", "int8_accumulate", "int8_dequant", "int8_matmul", "int8_abs_sum",
 ]

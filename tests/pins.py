@@ -14,13 +14,17 @@ What the checks compare against (never the oracle's own formulas):
   weight decoded independently (torch for E4M3, the golden table for E2M1,
   nibbles and block scales indexed element by element);
 * invariants the method states: the scale fold is exact, the GEMV is the M = 1
-  row of the GEMM, grouped equals per-group dense products, -1 writes zeros.
+  row of the GEMM, grouped equals per-group dense products, -1 writes zeros;
+* for the W8A8 int8 method: a hand-worked example, and scalar re-statements
+  in plain Python (integer sums; float32 rounding through ``struct``) of the
+  quantizer and the dequant.
 """
 
 from __future__ import annotations
 
 import math
 import os
+import struct
 from fractions import Fraction
 
 import numpy as np
@@ -516,6 +520,105 @@ def check_nvfp4_grouped_vs_dense(orc, seed=17):
                 assert np.isclose(got[r, col], scales[ex] * acc, rtol=1e-12, atol=1e-300)
 
 
+# ---------------------------------------------------------------- W8A8 int8 --
+
+def _f32(v: float) -> float:
+    """Round a Python float (binary64) to the nearest binary32 (ties to even)."""
+    return struct.unpack("<f", struct.pack("<f", v))[0]
+
+
+def check_int8_worked(orc):
+    rows = _rows("int8_w8a8_worked.txt")
+    x = np.array([[float(v) for v in r] for r in rows["x"]])
+    want_q = np.array([[int(v) for v in r] for r in rows["q"]], dtype=np.int8)
+    absmax = [float(v) for v in rows["absmax"][0]]
+    q, scale = orc.int8_quantize_rows(x)
+    assert np.array_equal(q, want_q), q
+    for i, am in enumerate(absmax):
+        assert scale[i] == np.float32(_f32(am / 127.0)), (i, scale[i])
+    assert scale[1] == 1.0 and scale[2] == 0.0
+    b = np.array([[int(v) for v in r] for r in rows["b"]], dtype=np.int8)
+    acc = orc.int8_accumulate(q, b)
+    want_acc = np.array([[int(v) for v in r] for r in rows["acc"]])
+    assert np.array_equal(acc, want_acc), acc
+    b_scale = np.array([float(v) for v in rows["b_scale"][0]], dtype=np.float32)
+    bias = np.array([float(v) for v in rows["bias"][0]])
+    out = orc.int8_matmul(q, b, scale, b_scale, bias).astype(np.float64)
+    want = np.array([[float(v) for v in r] for r in rows["out"]])
+    assert np.array_equal(out[1:], want[1:]), out
+    assert np.allclose(out[0], want[0], rtol=4 * 2.0 ** -24, atol=0), out
+
+
+def check_int8_quantizer_scalar(orc, seed=31):
+    """The quantizer equals a plain-Python restatement: absmax, scale =
+    absmax / 127 and x / scale each rounded once to binary32 (a binary64
+    result rounded to binary32 is the correctly rounded binary32 result for
+    a quotient of binary32 values), Python's round (half to even), clamp."""
+    rng = np.random.default_rng(seed)
+    bits, _ = _bf16_values(rng, (6, 40))
+    # a row whose absmax is 127 (scale 1) with exact halves, and a zero row
+    xv = orc.bf16_bits_to_f64(bits)
+    xv[4] = 0.0
+    xv[5, :8] = [127.0, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5, -126.5]
+    xv[5, 8:] = np.round(xv[5, 8:] * 8) / 8
+    q, scale = orc.int8_quantize_rows(xv)
+    for i in range(xv.shape[0]):
+        am = max(abs(float(v)) for v in xv[i])
+        s = _f32(am / 127.0)
+        assert float(scale[i]) == s, (i, scale[i], s)
+        for j in range(xv.shape[1]):
+            if s == 0.0:
+                want = 0
+            else:
+                want = max(-127, min(127, round(_f32(float(xv[i, j]) / s))))
+            assert int(q[i, j]) == want, (i, j, int(q[i, j]), want)
+
+
+def check_int8_quantizer_invariants(orc, seed=32):
+    """|q| <= 127; the absmax element gets +-127; x - q * scale is at most half
+    a step; q(-x) = -q(x)."""
+    rng = np.random.default_rng(seed)
+    bits, _ = _bf16_values(rng, (5, 64))
+    xv = orc.bf16_bits_to_f64(bits)
+    q, scale = orc.int8_quantize_rows(xv)
+    qn, scale_n = orc.int8_quantize_rows(-xv)
+    assert np.array_equal(scale, scale_n) and np.array_equal(qn, -q)
+    assert np.all(np.abs(q.astype(np.int64)) <= 127)
+    for i in range(xv.shape[0]):
+        j = int(np.argmax(np.abs(xv[i])))
+        assert abs(int(q[i, j])) == 127
+        err = np.abs(xv[i] - q[i].astype(np.float64) * float(scale[i]))
+        assert np.all(err <= 0.5 * float(scale[i]) * (1 + 2.0 ** -20)), err.max()
+
+
+def check_int8_product_scalar(orc, seed=33):
+    """The exact sums equal Python integer loops; the dequant equals the
+    float32 steps (acc * a_scale) * b_scale + bias done one by one through
+    ``struct``; sums beyond 2^24 (K = 1100, all codes +-127) round once."""
+    rng = np.random.default_rng(seed)
+    m, n, k = 8, 16, 9
+    qa = rng.integers(-127, 128, size=(m, k), dtype=np.int8)
+    qb = rng.integers(-127, 128, size=(n, k), dtype=np.int8)
+    sa = (rng.random(m) * 0.02).astype(np.float32)
+    sb = (rng.random(n) * 0.01).astype(np.float32)
+    bias = np.round(rng.standard_normal(n) * 8) / 8
+    acc = orc.int8_accumulate(qa, qb)
+    out = orc.int8_dequant(acc, sa, sb, bias)
+    for i in range(m):
+        for j in range(n):
+            s = sum(int(qa[i, c]) * int(qb[j, c]) for c in range(k))
+            assert int(acc[i, j]) == s
+            v = _f32(_f32(_f32(float(s)) * float(sa[i])) * float(sb[j]))
+            v = _f32(v + float(bias[j]))
+            assert float(out[i, j]) == v, (i, j, float(out[i, j]), v)
+    big_a = np.full((1, 1100), 127, dtype=np.int8)
+    big_b = np.full((1, 1100), -127, dtype=np.int8)
+    big_b[0, 0] = 126
+    s = 126 * 127 - 1099 * 127 * 127
+    assert int(orc.int8_accumulate(big_a, big_b)[0, 0]) == s
+    assert float(orc.int8_dequant(np.array([[s]]), [1.0], [1.0])[0, 0]) == _f32(float(s))
+
+
 ALL_CHECKS = [
     check_e4m3_table, check_e2m1_table, check_bf16_exactness, check_bf16_rounding,
     check_bf16_decode, check_fp8_worked, check_nvfp4_worked, check_grouped_worked,
@@ -523,4 +626,6 @@ ALL_CHECKS = [
     check_fp8_materialize_independent, check_scale_fold, check_gemv_is_gemm_row,
     check_grouped_vs_dense, check_tolerance_shape, check_f16_decode, check_f16_rounding,
     check_activations, check_epilogue, check_nvfp4_grouped_worked, check_nvfp4_grouped_vs_dense,
+    check_int8_worked, check_int8_quantizer_scalar, check_int8_quantizer_invariants,
+    check_int8_product_scalar,
 ]

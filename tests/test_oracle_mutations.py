@@ -14,6 +14,7 @@ import oracle
 import oracle.decode
 import oracle.formats
 import oracle.layer
+import oracle.w8a8
 from tests import pins
 
 
@@ -125,7 +126,55 @@ def _epilogue_act_first(v, bias=None, act="none"):
     return out if bias is None else out + np.asarray(bias, dtype=np.float64)
 
 
+def _int8_quant_ties_away(x):
+    xf = oracle.w8a8._as_values(x).astype(np.float32)
+    absmax = np.max(np.abs(xf), axis=1)
+    scale = (absmax / np.float32(127.0)).astype(np.float32)
+    q = np.zeros(xf.shape, dtype=np.int8)
+    nz = scale > 0
+    r = (xf[nz] / scale[nz][:, None]).astype(np.float32)
+    q[nz] = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    return q, scale
+
+
+def _int8_quant_scale_128(x):
+    xf = oracle.w8a8._as_values(x).astype(np.float32)
+    absmax = np.max(np.abs(xf), axis=1)
+    scale = (absmax / np.float32(128.0)).astype(np.float32)
+    q = np.zeros(xf.shape, dtype=np.int8)
+    nz = scale > 0
+    q[nz] = np.clip(np.rint(xf[nz] / scale[nz][:, None]), -127, 127).astype(np.int8)
+    return q, scale
+
+
+def _int8_dequant_scales_first(acc, a_scale, b_scale, bias=None):
+    f32 = np.float32
+    s = (np.asarray(a_scale, dtype=f32)[:, None] * np.asarray(b_scale, dtype=f32)[None, :]).astype(f32)
+    v = (np.asarray(acc).astype(f32) * s).astype(f32)
+    if bias is not None:
+        v = (v + np.asarray(bias, dtype=np.float64).astype(f32)[None, :]).astype(f32)
+    return v
+
+
+def _int8_dequant_no_b_scale(acc, a_scale, b_scale, bias=None):
+    return ORIG_INT8_DEQ(acc, a_scale, np.ones_like(np.asarray(b_scale, dtype=np.float32)), bias)
+
+
+def _int8_dequant_bias_first(acc, a_scale, b_scale, bias=None):
+    if bias is None:
+        return ORIG_INT8_DEQ(acc, a_scale, b_scale)
+    b = np.asarray(bias, dtype=np.float64).astype(np.float32)
+    return ORIG_INT8_DEQ(np.asarray(acc).astype(np.float32) + b[None, :], a_scale, b_scale)
+
+
+def _int8_accumulate_int16(q_a, q_b):
+    a = np.asarray(q_a, dtype=np.int8).astype(np.int16)
+    b = np.asarray(q_b, dtype=np.int8).astype(np.int16)
+    return (a @ b.T).astype(np.int64)
+
+
 ORIG_F16 = oracle.formats._one_f64_to_f16
+ORIG_INT8_DEQ = oracle.w8a8.int8_dequant
 ORIG_ACT = oracle.layer.activation
 ORIG_DECODE_NVFP4 = oracle.decode.decode_nvfp4
 ORIG_LINEAR = oracle.layer.linear
@@ -150,6 +199,17 @@ MUTATIONS = {
                         (oracle, "activation", _silu_wrong_sign)],
     "activation_before_bias": [(oracle.layer, "epilogue", _epilogue_act_first),
                                (oracle, "epilogue", _epilogue_act_first)],
+    "int8_quant_ties_away": [(oracle, "int8_quantize_rows", _int8_quant_ties_away)],
+    "int8_quant_scale_128": [(oracle, "int8_quantize_rows", _int8_quant_scale_128)],
+    "int8_dequant_scales_multiplied_first": [
+        (oracle.w8a8, "int8_dequant", _int8_dequant_scales_first),
+        (oracle, "int8_dequant", _int8_dequant_scales_first)],
+    "int8_dequant_no_b_scale": [(oracle.w8a8, "int8_dequant", _int8_dequant_no_b_scale),
+                                (oracle, "int8_dequant", _int8_dequant_no_b_scale)],
+    "int8_bias_before_dequant": [(oracle.w8a8, "int8_dequant", _int8_dequant_bias_first),
+                                 (oracle, "int8_dequant", _int8_dequant_bias_first)],
+    "int8_sum_in_int16": [(oracle.w8a8, "int8_accumulate", _int8_accumulate_int16),
+                          (oracle, "int8_accumulate", _int8_accumulate_int16)],
 }
 
 
