@@ -3,7 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--headline-only] [--no-cpu-baseline]
-                    [--only nvfp4|gemm|grouped|gemv-shapes]
+                    [--only nvfp4|gemm|grouped|w8a8|gemv-shapes]
 
 Prints ONE JSON line (rank 0).  The headline `value` is the M=1 FP8 (W8A16)
 decode GEMV throughput in GB/s of algorithmic bytes over one step = the three
@@ -416,6 +416,8 @@ def run_subs(args, gq, dev, stream, peaks, world, only=None):
         gemm_sub(gq, dev, stream, peaks, world, gsteps, warm, subs)
     if only in (None, "grouped"):
         grouped_sub(gq, dev, stream, peaks, world, gsteps, warm, subs)
+    if only in (None, "w8a8"):
+        w8a8_sub(gq, dev, stream, peaks, world, gsteps, warm, subs)
     return subs
 
 
@@ -493,6 +495,46 @@ def gemm_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
                                     "frac_bf16_tensor": round(tfl / peaks["bf16_tflops"], 4),
                                     "l2": f"{copies} rotating input copies"}
     del ins2
+
+
+def w8a8_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
+    """W8A8 int8 (the sibling method): per-row activation quantization of
+    x [2048, 4096] bf16, then the int8 GEMM with W [14336, 4096] int8."""
+    import synth
+    m, n, k = 2048, 14336, 4096
+    qb, sb = synth.int8_weight(n, k, seed=0)
+    x = synth.bf16_activations(m, k, seed=1)
+    copies = max(2, int(math.ceil(2 * L2_BYTES / (n * k + 2 * m * k))))
+    ins = [(x.to(dev), qb.to(dev)) for _ in range(copies)]
+    d_sb = sb.to(dev)
+    qa = torch.empty((m, k), dtype=torch.int8, device=dev)
+    sa = torch.empty((m,), dtype=torch.float32, device=dev)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+    def quant_step(i):
+        gq.int8_quantize_rows(ins[i % copies][0], q=qa, scale=sa, stream=stream)
+
+    def gemm_step(i):
+        gq.int8_matmul(qa, ins[i % copies][1], sa, d_sb, out=out, stream=stream)
+
+    def both_step(i):
+        quant_step(i)
+        gemm_step(i)
+
+    tq = graph_timer(quant_step, gsteps, warm, gsteps, stream, world) * 1e-3 / gsteps
+    tg = graph_timer(gemm_step, gsteps, warm, gsteps, stream, world) * 1e-3 / gsteps
+    tb = graph_timer(both_step, gsteps, warm, gsteps, stream, world) * 1e-3 / gsteps
+    qbytes = 2 * m * k + m * k + 4 * m
+    tfl = 2 * m * n * k / tg / 1e12
+    subs["int8_w8a8_m2048"] = {
+        "quantize_us": round(tq * 1e6, 2),
+        "quantize_GB/s": round(qbytes / tq / 1e9, 1),
+        "quantize_frac_hbm": round(qbytes / tq / 1e9 / peaks["hbm_gbs"], 4),
+        "gemm_us": round(tg * 1e6, 2), "gemm_TFLOP/s": round(tfl, 1),
+        "gemm_frac_bf16_tensor": round(tfl / peaks["bf16_tflops"], 4),
+        "step_us": round(tb * 1e6, 2),
+        "l2": f"{copies} rotating input copies"}
+    del ins
 
 
 def grouped_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
@@ -634,7 +676,7 @@ def main():
     ap.add_argument("--overlap-weight-reads", action="store_true",
                     help="GEMVs overlap their weight reads with the previous kernel "
                          "(GQ_LAUNCH_OVERLAP_WEIGHT_READS; weights are not written between launches)")
-    ap.add_argument("--only", choices=["nvfp4", "gemm", "grouped", "gemv-shapes"], default=None,
+    ap.add_argument("--only", choices=["nvfp4", "gemm", "grouped", "w8a8", "gemv-shapes"], default=None,
                     help="run one sub-benchmark alone and print its result (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

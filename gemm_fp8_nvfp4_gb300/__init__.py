@@ -11,8 +11,8 @@ the calls raise.
 
 Entry points (same names as the C ABI without the ``gq_`` prefix):
 ``fp8_gemv``, ``nvfp4_gemv``, ``fp8_matmul``, ``nvfp4_matmul``,
-``fp8_grouped_matmul``, ``nvfp4_grouped_matmul``, ``fp8_materialize``,
-``nvfp4_materialize``.  The
+``fp8_grouped_matmul``, ``nvfp4_grouped_matmul``, ``int8_quantize_rows``,
+``int8_matmul``, ``fp8_materialize``, ``nvfp4_materialize``.  The
 product calls take ``bias=`` and ``activation=`` for the fused epilogue
 (``out = act(alpha * acc + bias)``); with either given they call the ``_ex``
 form of the C entry point.  Outputs may be float32, bfloat16 or float16.
@@ -60,6 +60,9 @@ SIGNATURES = {
                                      _I64, _I64, _P]),
     "gq_nvfp4_grouped_matmul_ex": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
                                         _I64, _I64, _I64, _E, _P]),
+    "gq_int8_quantize_rows": (_I, [_P, _P, _P, _I64, _I64, _P]),
+    "gq_int8_matmul": (_I, [_P, _I, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "gq_int8_matmul_ex": (_I, [_P, _I, _P, _P, _P, _P, _I64, _I64, _I64, _E, _P]),
     "gq_fp8_materialize": (_I, [_P, _I, _P, _I64, _I64, _P]),
     "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
@@ -348,6 +351,47 @@ def nvfp4_grouped_matmul(a, q, bs, a_offsets, expert_ids, expert_scales=None,
     return c
 
 
+def int8_quantize_rows(x, q=None, scale=None, stream=None):
+    """W8A8 activation side: x [M, K] bf16 -> (q [M, K] int8, scale [M] float32),
+    scale = absmax / 127 per row, q = round-half-even(x / scale)."""
+    xp = _dev(x, "x", torch.bfloat16, 2)
+    m, k = x.shape
+    q = _out(q, (m, k), torch.int8, x.device)
+    scale = _out(scale, (m,), torch.float32, x.device)
+    st = load_library().gq_int8_quantize_rows(_dev(q, "q"), _dev(scale, "scale"), xp, m, k,
+                                              _stream_handle(stream))
+    _check(st, "int8_quantize_rows")
+    return q, scale
+
+
+def int8_matmul(a, b, a_scale, b_scale, out=None, out_dtype=torch.bfloat16, stream=None,
+                bias=None, activation="none"):
+    """W8A8 GEMM: c[M, N] = act((sum_k a[m,k] b[n,k]) * a_scale[m] * b_scale[n] + bias[n]);
+    a [M, K] int8, b [N, K] int8, a_scale [M], b_scale [N] float32."""
+    ap = _dev(a, "a", torch.int8, 2)
+    bp = _dev(b, "b", torch.int8, 2)
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k:
+        raise ValueError("a and b disagree on K")
+    sap = _dev(a_scale, "a_scale", torch.float32, 1)
+    sbp = _dev(b_scale, "b_scale", torch.float32, 1)
+    if a_scale.numel() != m or b_scale.numel() != n:
+        raise ValueError("a_scale must have M entries and b_scale N")
+    dtype = out.dtype if out is not None else out_dtype
+    c = _out(out, (m, n), dtype, a.device)
+    ep = _epilogue(bias, activation, (n,))
+    lib = load_library()
+    if ep is None:
+        st = lib.gq_int8_matmul(_dev(c, "out"), _out_code(dtype), ap, bp, sap, sbp, m, n, k,
+                                _stream_handle(stream))
+    else:
+        st = lib.gq_int8_matmul_ex(_dev(c, "out"), _out_code(dtype), ap, bp, sap, sbp, m, n, k,
+                                   _ref(ep), _stream_handle(stream))
+    _check(st, "int8_matmul")
+    return c
+
+
 def fp8_materialize(w, out=None, out_dtype=torch.bfloat16, stream=None):
     """Dense e4m3(w) [N, K] as float32, bf16 or float16 (exact, unscaled)."""
     w, wp = _u8(w, "w", 2)
@@ -392,7 +436,7 @@ def device_status(reset: bool = False) -> int:
 
 __all__ = [
     "fp8_gemv", "nvfp4_gemv", "fp8_matmul", "nvfp4_matmul", "fp8_grouped_matmul",
-    "nvfp4_grouped_matmul",
+    "nvfp4_grouped_matmul", "int8_quantize_rows", "int8_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
     "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
     "SIGNATURES", "LIB_PATH", "version", "status_str", "ACTIVATIONS", "Epilogue",

@@ -317,6 +317,42 @@ int gq_nvfp4_grouped_matmul(void* c_out, int out_dtype, const void* a, const uin
                                     nullptr, stream);
 }
 
+int gq_int8_quantize_rows(int8_t* q, float* scale, const void* x, int64_t M, int64_t K,
+                          cudaStream_t stream) {
+  if (M < 0 || K < 0) return GQ_ERR_SHAPE;
+  if (M == 0) return GQ_OK;
+  if (!scale || (K > 0 && (!q || !x))) return GQ_ERR_NULL;
+  if (!aligned(x, 2) || !aligned(scale, 4)) return GQ_ERR_ALIGN;
+  if (M > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  gq::Ctx c;
+  if (int s = gq::device_ctx(stream, &c)) return s;
+  return gq::launch_status(gq::launch_int8_quantize_rows(c, q, scale, x, M, K));
+}
+
+int gq_int8_matmul_ex(void* c_out, int out_dtype, const int8_t* a, const int8_t* b,
+                      const float* a_scale, const float* b_scale, int64_t M, int64_t N,
+                      int64_t K, const gq_epilogue* epilogue, cudaStream_t stream) {
+  if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;
+  if (M < 0 || N < 0 || K < 0 || K % 16 != 0) return GQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!c_out || !a_scale || !b_scale || (K > 0 && (!a || !b))) return GQ_ERR_NULL;
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c_out, 16) || !aligned(a_scale, 4) ||
+      !aligned(b_scale, 4))
+    return GQ_ERR_ALIGN;
+  if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  gq::Epi ep;
+  if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
+  gq::Ctx c;
+  if (int s = gq::device_ctx(stream, &c)) return s;
+  return gq::launch_status(gq::launch_int8_gemm(c, c_out, ep, a, b, a_scale, b_scale, M, N, K));
+}
+
+int gq_int8_matmul(void* c_out, int out_dtype, const int8_t* a, const int8_t* b,
+                   const float* a_scale, const float* b_scale, int64_t M, int64_t N, int64_t K,
+                   cudaStream_t stream) {
+  return gq_int8_matmul_ex(c_out, out_dtype, a, b, a_scale, b_scale, M, N, K, nullptr, stream);
+}
+
 int gq_fp8_materialize(void* out, int out_dtype, const uint8_t* w, int64_t N, int64_t K,
                        cudaStream_t stream) {
   if (!valid_dtype(out_dtype)) return GQ_ERR_DTYPE;

@@ -231,7 +231,7 @@ __device__ __forceinline__ bool epi_plain(const Epi& e) {
 // v = alpha * acc already; adds bias element bias_idx (when there is a bias)
 // and applies the activation.
 __device__ __forceinline__ float epi_apply(const Epi& e, float v, int64_t bias_idx) {
-  if (e.bias != nullptr) v += epi_bias(e, bias_idx);
+  if (e.bias != nullptr) v = __fadd_rn(v, epi_bias(e, bias_idx));   // never fused with a product
   if (e.act != kActNone) v = epi_act_call(e.act, v);
   return v;
 }

@@ -83,7 +83,9 @@ constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
 constexpr uint32_t kAHalfBytes = UMMA_M * BK * 2;  // 16 KB: offset of the second A half
 constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
 
-enum class Fmt { kFp8, kNvfp4 };
+// kInt8: the W8A8 sibling method (both operands int8, per-row / per-column
+// scales), run on the same pipeline with both operands widened to binary16.
+enum class Fmt { kFp8, kNvfp4, kInt8 };
 
 template <Fmt F> struct RawLayout;
 template <> struct RawLayout<Fmt::kFp8> {
@@ -94,11 +96,18 @@ template <> struct RawLayout<Fmt::kNvfp4> {
   static constexpr uint32_t kWBytes = BN * BK / 2;      // 8 KB, 32-byte swizzle
   static constexpr uint32_t kScaleBytes = BN * BK / 16; // 1 KB, 4 bytes per row
 };
+template <> struct RawLayout<Fmt::kInt8> {
+  static constexpr uint32_t kWBytes = BN * BK;          // 16 KB, 64-byte swizzle
+  static constexpr uint32_t kScaleBytes = 0;
+};
 
 template <Fmt F> struct Smem {
   static constexpr int kRawSt = kRawStages;     // A + raw weight ring
   static constexpr int kDeqSt = kDeqStages;     // decoded weight ring
   static constexpr uint32_t kAStride = kABytes;
+  static constexpr uint32_t kARawBytes = kABytes;   // A bytes the TMA brings per stage
+  static constexpr bool kADeq = false;              // A read by the MMA from the A ring
+  static constexpr uint32_t kDeqAOff = 0;
   static constexpr uint32_t kDeqStride = kDeqBytes;
   static constexpr uint32_t kDeqOff = 0;
   static constexpr uint32_t kAOff = kDeqOff + kDeqStages * kDeqBytes;
@@ -135,6 +144,9 @@ struct SmemAnyK {
   static constexpr uint32_t kPartWOff = kPartAOff + 1024;             // <= 15 rows of W
   static constexpr uint32_t kStage = (kPartWOff + 1280 + 1023) & ~1023u;
   static constexpr uint32_t kAStride = kStage;
+  static constexpr uint32_t kARawBytes = kABytes;
+  static constexpr bool kADeq = false;
+  static constexpr uint32_t kDeqAOff = 0;
   static constexpr uint32_t kDeqStride = kStage;
   static constexpr uint32_t kBarOff = 2 * kStage;
   static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
@@ -149,7 +161,30 @@ struct SmemAnyK {
 template <Fmt F, bool kAnyK>
 using SmemFor = typename std::conditional<kAnyK, SmemAnyK, Smem<F>>::type;
 
-static_assert(UMMA_M * kPartStride <= Smem<Fmt::kNvfp4>::kBarOff &&
+// W8A8: raw int8 A and W stages (16 KB each, 64-byte swizzle) and decoded
+// stages holding both operands as binary16 (W at +0, A at +32 KB).
+template <> struct Smem<Fmt::kInt8> {
+  static constexpr int kRawSt = kRawStages;
+  static constexpr int kDeqSt = kDeqStages;
+  static constexpr uint32_t kARawBytes = BM * BK;             // 16 KB of int8 A
+  static constexpr uint32_t kAStride = kARawBytes;
+  static constexpr bool kADeq = true;                         // MMA reads A from the decoded stage
+  static constexpr uint32_t kDeqAOff = kDeqBytes;
+  static constexpr uint32_t kDeqStride = kDeqBytes + kABytes; // 64 KB
+  static constexpr uint32_t kDeqOff = 0;
+  static constexpr uint32_t kAOff = kDeqOff + kDeqStages * kDeqStride;
+  static constexpr uint32_t kWOff = kAOff + kRawStages * kAStride;
+  static constexpr uint32_t kSOff = kWOff + kRawStages * RawLayout<Fmt::kInt8>::kWBytes;
+  static constexpr uint32_t kBarOff = kSOff;
+  static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kTotal = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kTotal + 1024;
+};
+static_assert(Smem<Fmt::kInt8>::kAlloc <= 232448, "W8A8 stages fit in shared memory");
+
+static_assert(UMMA_M * kPartStride <= Smem<Fmt::kInt8>::kBarOff &&
+              UMMA_M * kPartStride <= Smem<Fmt::kNvfp4>::kBarOff &&
                   UMMA_M * kPartStride <= Smem<Fmt::kFp8>::kBarOff &&
                   UMMA_M * kPartStride <= SmemAnyK::kBarOff,
               "split-K partials fit below the barriers");
@@ -169,7 +204,9 @@ struct Problem {
   int G, E, max_rows;          // grouped only
   int a_groups, w_groups;      // any-K path: full 8-row groups of A, 16-row groups of W
   Epi ep;                      // output type and fused epilogue
-  const void* a_g;             // any-K path: A [M, K] bf16 (read with plain loads)
+  const float* a_scale;        // W8A8: per-row scale of A [M]
+  const float* b_scale;        // W8A8: per-output-column scale of W [N]
+  const void* a_g;             // any-K path: A [M, K] bf16
   const uint8_t* w_g;          // any-K path: W [N, K] e4m3 codes
   int ksplit;                  // > 1: split-K over a thread-block cluster of ksplit CTAs
   int kb_per_split;            // K steps per split
@@ -396,7 +433,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // (grouped: every expert's weight streams from DRAM once).
     auto prefetch_w = [&](const Tile& pt, int pkb) {
       if (lane != 0 || !pt.valid || pt.expert < 0) return;
-      constexpr int kBpk = (F == Fmt::kFp8) ? BK : BK / 2;   // weight bytes per row per K step
+      constexpr int kBpk = (F == Fmt::kNvfp4) ? BK / 2 : BK;   // weight bytes per row per K step
       if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * kBpk, pt.n0, pt.expert);
       else tc::tma_prefetch_l2_2d(&tmap_w, pkb * kBpk, pt.n0);
     };
@@ -418,12 +455,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           ok = false;
           break;
         }
-        uint8_t* a_dst = smem + L::kAOff + s * kABytes;
+        uint8_t* a_dst = smem + L::kAOff + s * L::kAStride;
         uint8_t* w_dst = smem + L::kWOff + s * RawLayout<F>::kWBytes;
         if (lane == 0) {
-          tc::mbar_arrive_expect_tx(&full_raw[s], kABytes + RawLayout<F>::kWBytes);
+          tc::mbar_arrive_expect_tx(&full_raw[s], L::kARawBytes + RawLayout<F>::kWBytes);
           tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0);
-          constexpr int kBpk = (F == Fmt::kFp8) ? BK : BK / 2;
+          constexpr int kBpk = (F == Fmt::kNvfp4) ? BK / 2 : BK;
           if constexpr (kGrouped) tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0, tl.expert);
           else tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0);
         }
@@ -558,7 +595,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
-    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(UMMA_M, BN);
+    constexpr uint32_t kIdesc =
+        F == Fmt::kInt8 ? tc::idesc_f16_f32(UMMA_M, BN) : tc::idesc_bf16_f32(UMMA_M, BN);
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     int it = 0;
@@ -581,7 +619,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         tc::tc_fence_after();
         if (lane == 0) {
-          const uint32_t a_addr = smem_base + L::kAOff + s * L::kAStride;
+          const uint32_t a_addr = L::kADeq ? smem_base + L::kDeqOff + d * L::kDeqStride + L::kDeqAOff
+                                           : smem_base + L::kAOff + s * L::kAStride;
           const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -722,8 +761,29 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           break;
         }
         const uint32_t w_addr = smem_base + L::kWOff + s * RawLayout<F>::kWBytes;
-        const uint32_t b_addr = smem_base + L::kDeqOff + d * kDeqBytes;
-        if constexpr (F == Fmt::kFp8) {
+        const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
+        if constexpr (F == Fmt::kInt8) {
+          // Rows of 64 int8 codes (TMA 64-byte swizzle: chunk c at
+          // c ^ ((row >> 1) & 3)) -> binary16, exactly: the weight row, and
+          // the A row when the MMA reads it (a tile of at most 128 rows uses
+          // the first half only).
+          const uint32_t a_raw = smem_base + L::kAOff + s * L::kAStride;
+          const uint32_t a_dq = b_addr + L::kDeqAOff;
+          const bool do_a = row < UMMA_M || tl.m_end - tl.m0 > UMMA_M;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t src = row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
+            uint4 lo, hi;
+            s8x16_to_f16(tc::lds128(w_addr + src), lo, hi);
+            tc::sts128(b_addr + sw128_off(row, 2 * c), lo);
+            tc::sts128(b_addr + sw128_off(row, 2 * c + 1), hi);
+            if (do_a) {
+              s8x16_to_f16(tc::lds128(a_raw + src), lo, hi);
+              tc::sts128(a_dq + sw128_off(row, 2 * c), lo);
+              tc::sts128(a_dq + sw128_off(row, 2 * c + 1), hi);
+            }
+          }
+        } else if constexpr (F == Fmt::kFp8) {
           // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -833,11 +893,23 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           tc::tmem_ld_32x32b_x32(taddr + c0, r);
           tc::tmem_wait_ld();
           const int n = tl.n0 + c0;
+          float v[32];
+          if constexpr (F == Fmt::kInt8) {
+            // (acc * a_scale[m]) * b_scale[n], each product rounded once; lane
+            // i loads b_scale of column n + i and the warp shares it (every
+            // lane of the warp is here: the row test comes after).
+            const float sbv = n + lane < p.N ? __ldg(p.b_scale + n + lane) : 0.f;
+            const float sa = row_ok ? __ldg(p.a_scale + m) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), sa), __shfl_sync(0xFFFFFFFFu, sbv, i));
+          }
           if (!row_ok || n >= p.N) continue;
           const int lim = min(32, p.N - n);
-          float v[32];
+          if constexpr (F != Fmt::kInt8) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+          }
           if (!plain_epi) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = epi_apply(p.ep, v[i], bias0 + n + (i < lim ? i : 0));
@@ -898,7 +970,14 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         const int m = tl.m0 + r;
         const int n = tl.n0 + c;
-        const float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+        if constexpr (F == Fmt::kInt8) {
+          const float sa = __ldg(p.a_scale + m);
+          const float in[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[i] = __fmul_rn(__fmul_rn(in[i], sa), __ldg(p.b_scale + min(n + i, p.N - 1)));
+        }
         const int64_t base = static_cast<int64_t>(m) * p.N + n;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -1052,6 +1131,23 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
   const int grid = plan_split(c, p, tiles);
   return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid);
+}
+
+cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_t* a,
+                             const int8_t* b, const float* a_scale, const float* b_scale,
+                             int64_t M, int64_t N, int64_t K) {
+  // K = 0: every sum is 0, so the output is the epilogue of 0.
+  if (K == 0) return fill_zero(c, out, ep, M * N, N, 0.f);
+  CUtensorMap ta, tw;
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  Problem p = base_problem(c, out, ep, M, N, K, 1.0f);
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
+  const int grid = plan_split(c, p, tiles);
+  return launch<Fmt::kInt8, false>(c, ta, tw, nullptr, p, grid);
 }
 
 // The grouped problem shared by both formats, and its persistent grid: an

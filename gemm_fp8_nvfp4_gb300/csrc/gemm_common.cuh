@@ -36,6 +36,30 @@ __device__ __forceinline__ void fp8x16_to_bf16(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// 16 int8 codes -> 16 binary16, exactly: each byte's sign bit is flipped
+// (u = code + 128, 0..255), the byte becomes the low byte of the binary16
+// 0x6400 | u = 1024 + u (spacing 1 in [1024, 2048)), and 1152 is subtracted
+// (exact: the result is the integer code in [-128, 127]).
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint32_t u, uint32_t sel) {
+  uint32_t h, d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(h) : "r"(u), "r"(0x64646464u), "r"(sel));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64806480u));
+  return d;
+}
+
+__device__ __forceinline__ void s8x16_to_f16(uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;
+    o[2 * i] = s8x2_to_f16x2(u, 0x5140u);       // codes 4i, 4i+1
+    o[2 * i + 1] = s8x2_to_f16x2(u, 0x5342u);   // codes 4i+2, 4i+3
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale
 // (given as f16 bits) -> 16 bf16, exact (the product has at most 6
 // significant bits and lies in [2^-10, 2688]).

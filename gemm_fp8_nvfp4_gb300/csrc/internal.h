@@ -80,6 +80,13 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                     int64_t E, int64_t max_rows,
                                     int64_t total_M, int64_t N, int64_t K);
 
+// W8A8: c = epilogue((acc * a_scale[m]) * b_scale[n]), acc = sum a[m,k] b[n,k].
+cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_t* a,
+                             const int8_t* b, const float* a_scale, const float* b_scale,
+                             int64_t M, int64_t N, int64_t K);
+// Per-row absmax int8 quantization of bf16 activations.
+cudaError_t launch_int8_quantize_rows(const Ctx& c, int8_t* q, float* scale, const void* x,
+                                      int64_t M, int64_t K);
 cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                       const void* a, const uint8_t* q,
                                       const uint8_t* bs, const uint32_t* a_offsets,

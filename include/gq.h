@@ -265,6 +265,44 @@ int gq_nvfp4_grouped_matmul_ex(void* c, int out_dtype, const void* a, const uint
                                const gq_epilogue* epilogue, cudaStream_t stream);
 
 /*
+ * W8A8 int8, activation side: per-row symmetric absmax quantization.
+ * Source: the "int8_matmul" page, enqueue_apple_int8_quantize_activation
+ * (A quantized online, one fp32 scale per row, scale = absmax / 127).
+ *     scale[m] = max_k |x[m, k]| / 127                      (float32 division)
+ *     q[m, k]  = clamp(rint(x[m, k] / scale[m]), -127, 127) (float32 division,
+ *                round half to even); a row of zeros: scale 0, codes 0.
+ *   x [M, K] bfloat16 (2-byte aligned; finite values), q [M, K] int8,
+ *   scale [M] float32 (4-byte aligned).  Any M, K; rows that are 16-byte
+ *   aligned with K % 16 == 0 and K <= 8192 are read once, others twice.
+ */
+int gq_int8_quantize_rows(int8_t* q, float* scale, const void* x, int64_t M, int64_t K,
+                          cudaStream_t stream);
+
+/*
+ * W8A8 int8 GEMM.  Source: the "int8_matmul" page, enqueue_apple_int8_matmul:
+ *     acc[m, n] = sum_k a[m, k] * b[n, k]           (exact integer products)
+ *     c[m, n]   = (acc * a_scale[m]) * b_scale[n]   (float32, each product
+ *                 rounded once), then the epilogue (bias after the dequant,
+ *                 activation), then the output conversion.
+ *   c [M, N] (out_dtype), a [M, K] int8, b [N, K] int8 (one row per output
+ *   column), a_scale [M], b_scale [N] float32.  K % 16 == 0.  a, b, c
+ *   16-byte aligned; scales 4-byte aligned.
+ * GB300 has no int8 tensor-core instruction on sm_103a (tcgen05 kind::i8
+ * is not available there), so both operands are widened exactly to binary16
+ * in shared memory and the sums are accumulated in float32: exact, and equal
+ * to the int32 sums, while every |partial sum| stays below 2^24 (always when
+ * sum_k |a[m,k] b[n,k]| < 2^24, e.g. K <= 1040); beyond that the sum is
+ * rounded to float32 precision.
+ */
+int gq_int8_matmul(void* c, int out_dtype, const int8_t* a, const int8_t* b,
+                   const float* a_scale, const float* b_scale, int64_t M, int64_t N,
+                   int64_t K, cudaStream_t stream);
+/* The same with a fused epilogue (see gq_epilogue; NULL = gq_int8_matmul). */
+int gq_int8_matmul_ex(void* c, int out_dtype, const int8_t* a, const int8_t* b,
+                      const float* a_scale, const float* b_scale, int64_t M, int64_t N,
+                      int64_t K, const gq_epilogue* epilogue, cudaStream_t stream);
+
+/*
  * FP8 materialize: out[n, k] = e4m3(w[n, k]) as float32, bfloat16 or binary16,
  * exact (every E4M3 value is representable in all three), no scale applied.
  * Source: "fp8_gemv" page -- enqueue_fp8_materialize / fp8_materialize_kernel.

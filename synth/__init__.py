@@ -123,6 +123,25 @@ def nvfp4_expert_stack(e: int, n: int, k: int, seed: int = 0, device="cpu"):
     return q.to(device), bs.to(device), s2.to(device)
 
 
+def int8_weight(n: int, k: int, seed: int = 0, device="cpu"):
+    """(codes int8 [n, k], scale float32 [n]): W ~ N(0, 0.02) quantized per
+    output row, symmetric absmax (scale = absmax / 127, round half to even)."""
+    w = gaussian((n, k), 0.02, seed)
+    absmax = w.abs().amax(dim=1)
+    scale = absmax / 127.0
+    safe = torch.where(scale > 0, scale, torch.ones_like(scale))
+    codes = torch.round(w / safe.unsqueeze(1)).clamp(-127, 127).to(torch.int8)
+    return codes.to(device), scale.to(device)
+
+
+def int8_codes(m: int, k: int, seed: int = 0, device="cpu"):
+    """(codes int8 [m, k] uniform in [-127, 127], scale float32 [m] in (0, 0.05])."""
+    g = _gen(seed)
+    codes = torch.randint(-127, 128, (m, k), generator=g, dtype=torch.int16).to(torch.int8)
+    scale = (torch.rand(m, generator=g) * 0.05 + 1e-4).to(torch.float32)
+    return codes.to(device), scale.to(device)
+
+
 def moe_routing(total_rows: int, seed: int = 2):
     """(a_offsets int64 [G+1], expert_ids int64 [G], counts [G]) for the
     9-category routing described in the module docstring."""

@@ -1,0 +1,162 @@
+"""W8A8 int8: the per-row activation quantizer and the int8 GEMM against the
+oracle.
+
+The quantizer takes its integer decisions in float32 like the oracle, so codes
+and scales are compared bit for bit.  The GEMM widens int8 exactly to binary16
+and sums in float32; where sum_k |a b| < 2^24 every partial sum is an exact
+integer, so the float32 dequant ((acc * a_scale) * b_scale, then bias) and the
+output rounding match the oracle bit for bit; beyond that the test allows the
+float32 accumulation error K * 2^-24 * sum|a b| (scaled) plus one output ulp.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_fp8_nvfp4_gb300 as gq
+import oracle
+import synth
+from tests.gpu_util import DEV, assert_canary, assert_exact, assert_within, bits, canary_out, lib, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def out_bits_f64(v32, out_dtype):
+    """Oracle float32 values -> the values of the output type, rounded RNE."""
+    v = np.asarray(v32, dtype=np.float64)
+    if out_dtype == torch.bfloat16:
+        return oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(v))
+    if out_dtype == torch.float16:
+        return oracle.f16_bits_to_f64(oracle.f64_to_f16_bits(v))
+    return v
+
+
+def check_quantize(m, k, seed, special=False):
+    x = synth.bf16_activations(m, k, seed=seed)
+    if special and m >= 3:
+        x[0] = 0
+        row = torch.zeros(k)
+        row[0] = 127
+        vals = torch.tensor([2.5, 3.5, -2.5, -0.5, 0.5, 1.5, -126.5])
+        row[1:1 + min(7, k - 1)] = vals[:min(7, k - 1)]
+        x[1] = row.to(torch.bfloat16)
+    q, s = gq.int8_quantize_rows(x.to(DEV))
+    torch.cuda.synchronize()
+    want_q, want_s = oracle.int8_quantize_rows(bits(x))
+    assert np.array_equal(q.cpu().numpy(), want_q), "codes differ"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32)), "scales differ"
+
+
+@pytest.mark.parametrize("m,k", [(1, 16), (3, 64), (257, 4096), (64, 8192), (5, 8208),
+                                 (7, 100), (33, 5), (2, 1)])
+def test_quantize_rows_exact(m, k):
+    lib()
+    check_quantize(m, k, seed=m + k, special=True)
+
+
+def test_quantize_rows_unaligned_rows():
+    """A row pitch that is not a multiple of 16 bytes takes the element-wise
+    kernel; a view starting 2 bytes in does too."""
+    lib()
+    x = synth.bf16_activations(9, 72, seed=3).to(DEV)
+    q, s = gq.int8_quantize_rows(x)
+    want_q, want_s = oracle.int8_quantize_rows(bits(x.cpu()))
+    assert np.array_equal(q.cpu().numpy(), want_q)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
+
+
+def run_matmul(qa, sa, qb, sb, out_dtype=torch.bfloat16, bias=None, act="none", rows=None):
+    m, n = qa.shape[0], qb.shape[0]
+    buf, c = canary_out((m, n), out_dtype)
+    gq.int8_matmul(qa.to(DEV), qb.to(DEV), sa.to(DEV), sb.to(DEV), out=c,
+                   bias=None if bias is None else bias.to(DEV), activation=act)
+    torch.cuda.synchronize()
+    assert_canary(buf)
+    got = to_f64(c)
+    sel = np.arange(m) if rows is None else np.asarray(rows)
+    qa_s, sa_s = qa.numpy()[sel], sa.numpy()[sel]
+    b64 = None if bias is None else oracle.bf16_bits_to_f64(bits(bias))
+    pre = oracle.int8_matmul(qa_s, qb.numpy(), sa_s, sb.numpy(), b64)
+    abs_sum = oracle.int8_abs_sum(qa_s, qb.numpy())
+    exact = bool(np.all(abs_sum < 2 ** 24))
+    if act == "none" and exact:
+        assert_exact(got[sel], out_bits_f64(pre, out_dtype), f"int8 {m}x{n}x{qa.shape[1]}")
+        return got
+    acc_err = qa.shape[1] * 2.0 ** -24 * abs_sum * (np.abs(sa_s)[:, None] * np.abs(sb.numpy())[None, :])
+    tol_pre = 0.0 if exact else acc_err
+    ref = oracle.epilogue(pre.astype(np.float64), None, act)
+    out_kind = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[out_dtype]
+    tol = oracle.tolerance_epilogue(tol_pre + 2.0 ** -22 * np.abs(pre), ref, act, out_kind)
+    assert_within(got[sel], ref, tol, f"int8 {m}x{n}x{qa.shape[1]} {act}")
+    return got
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 256, 16), (16, 4096, 4096), (128, 384, 256), (129, 257, 64),
+                                   (300, 1000, 2048), (512, 512, 1024), (3, 7, 32), (260, 96, 1040)])
+def test_int8_matmul_exact(m, n, k):
+    lib()
+    qa, sa = synth.int8_codes(m, k, seed=m + k)
+    qb, sb = synth.int8_weight(n, k, seed=n + k)
+    run_matmul(qa, sa, qb, sb)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_int8_matmul_out_types(out_dtype):
+    lib()
+    qa, sa = synth.int8_codes(200, 512, seed=1)
+    qb, sb = synth.int8_weight(320, 512, seed=2)
+    run_matmul(qa, sa, qb, sb, out_dtype)
+
+
+def test_int8_matmul_bias_exact_and_activations():
+    lib()
+    qa, sa = synth.int8_codes(140, 256, seed=4)
+    qb, sb = synth.int8_weight(272, 256, seed=5)
+    bias = synth.gaussian((272,), 0.1, seed=6).to(torch.bfloat16)
+    run_matmul(qa, sa, qb, sb, bias=bias)
+    for act in ("relu", "silu", "gelu_tanh"):
+        run_matmul(qa, sa, qb, sb, bias=bias, act=act)
+
+
+def test_int8_large_sums_within_bound():
+    """Uniform codes with K = 8192: sums of |a b| reach 2^25, beyond exact
+    float32 accumulation; the result stays within the accumulation bound."""
+    lib()
+    qa, sa = synth.int8_codes(130, 8192, seed=7)
+    qb, _ = synth.int8_codes(256, 8192, seed=8)
+    sb = torch.full((256,), 0.01, dtype=torch.float32)
+    run_matmul(qa, sa, qb, sb, out_dtype=torch.float32)
+
+
+def test_w8a8_pipeline_prefill_sampled():
+    """x [2048, 4096] bf16 -> quantize (bit-exact) -> int8 GEMM with the
+    [14336, 4096] int8 weight, bf16 out, checked on sampled rows."""
+    lib()
+    x = synth.bf16_activations(2048, 4096, seed=1)
+    qb, sb = synth.int8_weight(14336, 4096, seed=0)
+    qa_d, sa_d = gq.int8_quantize_rows(x.to(DEV))
+    qa, sa = oracle.int8_quantize_rows(bits(x))
+    assert np.array_equal(qa_d.cpu().numpy(), qa)
+    assert np.array_equal(sa_d.cpu().numpy().view(np.uint32), sa.view(np.uint32))
+    rng = np.random.default_rng(3)
+    rows = sorted(set([0, 1, 127, 128, 255, 2047] + list(rng.integers(0, 2048, 20))))
+    run_matmul(torch.from_numpy(qa), torch.from_numpy(sa), qb, sb, rows=rows)
+
+
+def test_int8_k_zero_and_errors():
+    lib()
+    l = gq.load_library()
+    s = torch.cuda.current_stream().cuda_stream
+    qa = torch.zeros((4, 0), dtype=torch.int8, device=DEV)
+    qb = torch.zeros((8, 0), dtype=torch.int8, device=DEV)
+    sa = torch.ones(4, device=DEV)
+    sb = torch.ones(8, device=DEV)
+    bias = torch.arange(8, dtype=torch.float32, device=DEV)
+    c = gq.int8_matmul(qa, qb, sa, sb, out_dtype=torch.float32, bias=bias)
+    assert torch.equal(c.cpu(), bias.cpu().expand(4, 8))
+    a = torch.zeros((4, 24), dtype=torch.int8, device=DEV)
+    c = torch.zeros((4, 8), dtype=torch.float32, device=DEV)
+    assert l.gq_int8_matmul(c.data_ptr(), 0, a.data_ptr(), a.data_ptr(), sa.data_ptr(),
+                            sb.data_ptr(), 4, 8, 24, s) == 2
+    assert l.gq_int8_matmul(c.data_ptr(), 0, a.data_ptr(), a.data_ptr(), None, sb.data_ptr(),
+                            4, 8, 16, s) == 1
