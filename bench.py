@@ -9,9 +9,10 @@ Prints ONE JSON line (rank 0).  The headline `value` is the M=1 FP8 (W8A16)
 decode GEMV throughput in GB/s of algorithmic bytes over one step = the three
 decode shapes (N, K) = (4096, 4096), (14336, 4096), (4096, 14336), bf16 output
 with the per-tensor scale folded.  The same line carries, under "sub", the
-other halves of the metric (NVFP4 GEMV GB/s, M=2048 W8A16 GEMM TFLOP/s) and
-the NVFP4 M=16/128 and grouped-MoE throughputs, each with its roofline
-fraction against MEASURED_PEAKS.json.
+other halves of the metric (NVFP4 GEMV GB/s, M=2048 W8A16 GEMM TFLOP/s), the
+NVFP4 M=16/128 GEMMs, the FP8 GEMM with K = 4100, the FP8 and NVFP4
+grouped-MoE GEMMs and the W8A8 int8 quantizer + GEMM, each with its
+roofline fraction against MEASURED_PEAKS.json.
 
 Timing: inputs are resident in HBM; the K timed steps run as CUDA-graph
 replays (a captured chunk of steps, replayed until exactly K steps ran),

@@ -19,11 +19,11 @@
 //   count; TN = 128 is used when 256-row tiles would leave SMs idle (with
 //   half the dequant work per step, two groups of dequant warps then work on
 //   alternate K steps).
-// * K is split over a thread-block cluster of S CTAs (S a power of two) so
-//   that ceil(N / TN) * S CTAs fill the GPU.  The fp32 partial tiles meet in
-//   distributed shared memory; rank r sums columns [r * TN / S, (r + 1) *
-//   TN / S) of the tile over the ranks in rank order (deterministic), scales,
-//   converts and stores them.
+// * K is split over a thread-block cluster of S <= 8 CTAs (any size whose
+//   clusters are all resident at once) so that ceil(N / TN) * S CTAs fill the
+//   GPU.  The fp32 partial tiles meet in distributed shared memory; rank r
+//   sums its slice of ceil(TN / S) columns (rounded up to 4) of the tile over
+//   the ranks in rank order (deterministic), scales, converts and stores them.
 // * Three rings, each released by its own consumer: the raw weight ring,
 //   freed as soon as its K steps are dequantized; the dequantized-weight
 //   ring, freed by the MMA; and the activation ring with its own TMA warp,
@@ -134,7 +134,7 @@ struct SkProblem {
   int M, N, K;
   int m_pad;           // activation rows loaded per stage: M rounded up to 8
   int nkb;             // K steps of BK
-  int ksplit;          // cluster size S (power of two, <= kMaxSplit; TN / S >= 16)
+  int ksplit;          // cluster size S (<= kMaxSplit)
   Epi ep;              // output type and fused epilogue
   int wp_box;          // inner box (bytes) of the weight prefetch map
 };
@@ -393,9 +393,10 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   __syncthreads();
   if (S > 1) tc::cluster_sync();
   {
-    // Rank r: columns [r * cols, (r + 1) * cols) of the tile, all M rows,
-    // four columns per task.
-    const int cols = TN / S;
+    // Rank r: columns [r * cols, min(TN, (r + 1) * cols)) of the tile, all
+    // M rows, four columns per task.
+    const int cols = ((TN + S - 1) / S + 3) / 4 * 4;
+    const int c_end = min(TN, (rank + 1) * cols);
     const int per_row = cols / 4;
     const int tasks = p.M * per_row;
     const bool vec = (p.N & 3) == 0;
@@ -403,7 +404,7 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       const int m = task / per_row;
       const int nl = rank * cols + 4 * (task % per_row);
       const int n = n0 + nl;
-      if (n >= p.N) continue;
+      if (nl >= c_end || n >= p.N) continue;
       const uint32_t addr = part + m * kPartStride + nl * 4;
       float4 acc;
       if (S == 1) {
@@ -490,16 +491,17 @@ int max_active_clusters(int device, int S) {
   return n;
 }
 
-// K split for TN-row tiles: the largest power of two S <= kMaxSplit such that
-// the tiles * S CTAs fit on the GPU in one wave (as clusters) and every rank
-// keeps at least kMinRawPerSplit raw stages.
+// K split for TN-row tiles: the largest S <= kMaxSplit such that the tiles *
+// S CTAs fit on the GPU in one wave (all clusters resident at once) and every
+// rank keeps at least kMinRawPerSplit raw stages.
 template <Fmt F, int TN>
 int plan_split(const Ctx& c, int tiles, int nkb) {
   const int nrs = (nkb + Raw<F>::kKbPer - 1) / Raw<F>::kKbPer;
-  int S = 1;
-  while (S < kMaxSplit && tiles * S * 2 <= c.num_sms && nrs >= S * 2 * kMinRawPerSplit) S *= 2;
-  while (S > 1 && max_active_clusters<F, TN>(c.device, S) < tiles) S /= 2;
-  return S;
+  for (int S = kMaxSplit; S > 1; --S) {
+    if (tiles * S > c.num_sms || nrs < S * kMinRawPerSplit) continue;
+    if (max_active_clusters<F, TN>(c.device, S) >= tiles) return S;
+  }
+  return 1;
 }
 
 // Tensor maps for TN-row tiles.  The weight rows are row_bytes long: raw
