@@ -337,6 +337,8 @@ def run_ours(args, rank, local, world):
     line["e2e"] = e2e_gemv(gq, base, dev, stream, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_gemv(args)
+        if not args.headline_only:
+            line["cpu_baseline"]["per_config"] = cpu_baseline_configs()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -613,6 +615,66 @@ def cpu_baseline_gemv(args, budget_s=12.0):
             "cores": cpu_threads(), "kind": "oracle",
             "sample": f"{steps} full step(s) of the three decode shapes in {dt:.1f} s "
                       f"(numpy float64 table decode + matvec)"}
+
+
+def cpu_baseline_configs():
+    """The oracle timed on the other workloads of the line (each a bounded,
+    stated sample), in the unit of the matching sub-result."""
+    import oracle
+    import synth
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    out = {}
+    n = k = 4096
+    q, bs, s2 = synth.nvfp4_weight(n, k, seed=0)
+    qn, bn = q.numpy(), bs.numpy()
+    for m in (1, 16, 128):
+        ab = synth.bf16_bits(synth.bf16_activations(m, k, seed=1))
+        dt = timed(lambda: oracle.nvfp4_matmul(ab, qn, bn, s2))
+        key = "nvfp4_gemv_m1" if m == 1 else f"nvfp4_gemm_m{m}"
+        if m < 128:
+            out[key] = {"value": round(nvfp4_bytes(m, n, k) / dt / 1e9, 3), "unit": "GB/s",
+                        "sample": f"the full product, {dt:.2f} s"}
+        else:
+            out[key] = {"value": round(2 * m * n * k / dt / 1e12, 5), "unit": "TFLOP/s",
+                        "sample": f"the full product, {dt:.2f} s"}
+    n2, rows = 14336, 16
+    codes, sc = synth.fp8_weight(n2, k, seed=0)
+    ab = synth.bf16_bits(synth.bf16_activations(rows, k, seed=1))
+    cn = codes.numpy()
+    dt = timed(lambda: oracle.fp8_matmul(ab, cn, sc))
+    out["fp8_gemm_m2048"] = {"value": round(2 * rows * n2 * k / dt / 1e12, 5), "unit": "TFLOP/s",
+                             "sample": f"{rows} of the 2048 rows against the full weight, {dt:.2f} s"}
+    qb, sb = synth.int8_weight(n2, k, seed=0)
+    xb = synth.bf16_bits(synth.bf16_activations(rows, k, seed=1))
+    qbn, sbn = qb.numpy(), sb.numpy()
+
+    def w8a8():
+        qa, sa = oracle.int8_quantize_rows(xb)
+        oracle.int8_matmul(qa, qbn, sa, sbn)
+
+    dt = timed(w8a8)
+    out["int8_w8a8_m2048"] = {"value": round(2 * rows * n2 * k / dt / 1e12, 5), "unit": "TFLOP/s",
+                              "sample": f"quantize + product of {rows} of the 2048 rows, {dt:.2f} s"}
+    stack, scales = synth.fp8_expert_stack(8, n2, k, seed=0)
+    offs, ids, _ = synth.moe_routing(4096, seed=2)
+    a_moe = synth.bf16_bits(synth.bf16_activations(4096, k, seed=1))
+    o = offs.numpy()
+    sample_rows = np.concatenate([np.arange(o[z], min(o[z] + 8, o[z + 1])) for z in (0, 1)])
+    st, scn, idn = stack.numpy(), scales.numpy(), ids.numpy()
+    dt = timed(lambda: oracle.fp8_grouped_matmul(a_moe, st, o, idn, scn, rows=sample_rows))
+    out["fp8_grouped_moe"] = {"value": round(2 * len(sample_rows) * n2 * k / dt / 1e12, 5),
+                              "unit": "TFLOP/s",
+                              "sample": f"{len(sample_rows)} rows of the first two groups "
+                                        f"(experts 0, 1), {dt:.2f} s"}
+    for v in out.values():
+        v["cores"] = cpu_threads()
+        v["kind"] = "oracle"
+    return out
 
 
 def run_reference(args, rank, local, world):
