@@ -160,3 +160,26 @@ def test_int8_k_zero_and_errors():
                             sb.data_ptr(), 4, 8, 24, s) == 2
     assert l.gq_int8_matmul(c.data_ptr(), 0, a.data_ptr(), a.data_ptr(), None, sb.data_ptr(),
                             4, 8, 16, s) == 1
+
+
+def test_quantize_exact_ties_and_tiny_rows():
+    """Rows whose quotients are exact half-integers (scale a power of two),
+    rows of tiny magnitude (the scale far below normal activations, down to
+    bf16 subnormals), and random rows: codes and scales bit-exact."""
+    lib()
+    k = 256
+    g = torch.Generator().manual_seed(9)
+    rows = []
+    for e in (-3, 0, 4):
+        s = 2.0 ** e
+        r = (torch.randint(-127, 127, (k,), generator=g).to(torch.float32) + 0.5) * s
+        r[0] = 127 * s
+        rows.append(r)
+    for e in (-100, -125, -133):
+        rows.append(torch.randn(k, generator=g) * 2.0 ** e)
+    rows.append(torch.randn(k, generator=g) * 1e3)
+    x = torch.stack(rows).to(torch.bfloat16)
+    q, s = gq.int8_quantize_rows(x.to(DEV))
+    want_q, want_s = oracle.int8_quantize_rows(bits(x))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), want_q)
