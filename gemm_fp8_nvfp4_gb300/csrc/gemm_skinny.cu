@@ -137,6 +137,7 @@ struct SkProblem {
   int ksplit;          // cluster size S (<= kMaxSplit)
   Epi ep;              // output type and fused epilogue
   int wp_box;          // inner box (bytes) of the weight prefetch map
+  int overlap_weights; // the weight producer reads before the previous kernel completes
 };
 
 template <Fmt F, int TN>
@@ -147,6 +148,12 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   using R = Raw<F>;
   using L = Smem<F, TN>;
   using C = TileCfg<TN>;
+  // Programmatic dependent launch: the next kernel in the stream may start
+  // its launch now; this one sets up (barriers, TMEM, descriptors) while the
+  // previous kernel finishes, and waits for it before any global access --
+  // except, with GQ_LAUNCH_OVERLAP_WEIGHT_READS, the weight producer, whose
+  // reads of the (unchanging) weights then overlap the previous kernel.
+  pdl_launch_dependents();
   constexpr int kRawStages = C::kRaw, kActStages = C::kAct, kDqStages = C::kDq, kGroups = C::kGroups;
   constexpr uint32_t kRawBytes = L::kRawBytes, kDeqBytes = L::kDeqBytes, kPartStride = L::kPartStride;
   extern __shared__ uint8_t smem_raw[];
@@ -213,6 +220,8 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const bool early_weights = p.overlap_weights && warp == kWarpW;
+  if (!early_weights) pdl_wait();
   const uint32_t part = smem_base;   // fp32 partial tile [m][TN n], over the rings
 
   if (warp == kWarpW) {
@@ -389,6 +398,7 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     }
   }
 
+  if (early_weights) pdl_wait();   // before this warp's part of the output stores
   tc::tc_fence_before();
   __syncthreads();
   if (S > 1) tc::cluster_sync();
@@ -541,13 +551,15 @@ cudaError_t launch_tn(const Ctx& c, SkProblem p, int S, const void* a, const uin
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Smem<F, TN>::kAlloc;
   cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = S > 1 ? 1 : 0;
+  cfg.numAttrs = S > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_wq_gemm_skinny<F, TN>, ta, tw, twp, ts, p);
 }
 
@@ -577,6 +589,7 @@ SkProblem make_problem(const Ctx& c, void* out, const Epi& ep, int64_t M, int64_
   p.nkb = static_cast<int>((K + BK - 1) / BK);
   p.ksplit = 1;
   p.ep = ep;
+  p.overlap_weights = c.overlap_weights ? 1 : 0;
   return p;
 }
 

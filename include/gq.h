@@ -104,18 +104,20 @@ typedef struct gq_epilogue {
  * Process-wide launch options (default 0).
  *
  * The GEMV entry points (gq_fp8_gemv, gq_nvfp4_gemv and their _ex forms)
+ * and the few-row GEMM (gq_fp8_matmul / gq_nvfp4_matmul with M <= 128)
  * always launch their kernel as a programmatic dependent of the previous
  * kernel in the stream; by default every thread waits for that kernel to
  * finish (and its writes to become visible) before it touches any global
- * memory, so stream order is unchanged and only the launch gap is hidden.
+ * memory, so stream order is unchanged and only the launch gap (and, for the
+ * GEMM, its set-up) is hidden.
  *
- * GQ_LAUNCH_OVERLAP_WEIGHT_READS: each GEMV thread issues its first weight
- * loads before that wait, and reads x and writes y only after it.  The weight
- * stream of a GEMV then overlaps the tail of the kernel before it, which is
- * what a decode loop over layers with fixed weights wants.  Only set it when
- * no kernel issued just before a GEMV writes that GEMV's weight buffers:
- * those reads are not ordered after the previous kernel.  Activations and
- * outputs always are.
+ * GQ_LAUNCH_OVERLAP_WEIGHT_READS: each GEMV thread, and the few-row GEMM's
+ * weight producer, issue their weight loads before that wait; activations
+ * are read and outputs written only after it.  The weight stream then
+ * overlaps the tail of the kernel before, which is what a decode loop over
+ * layers with fixed weights wants.  Only set it when no kernel issued just
+ * before such a call writes its weight buffers: those reads are not ordered
+ * after the previous kernel.  Activations and outputs always are.
  * Not a citation of the pages: a GB300 launch option.
  * gq_set_launch_flags returns GQ_ERR_SHAPE for unknown bits.
  */
