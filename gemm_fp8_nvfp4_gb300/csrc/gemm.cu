@@ -118,7 +118,11 @@ template <Fmt F> struct Smem {
   // (kDeqStages each), tmem_full, tmem_empty (2 each), drain (1)
   static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;   // tmem addr, abort flag
-  static constexpr uint32_t kTotal = kMiscOff + 16;
+  // Output staging for TMA stores: 2 buffers of a 32 x 32 16-bit box per
+  // epilogue warp (1 KB aligned, 64-byte swizzle).
+  static constexpr uint32_t kStageOff = (kMiscOff + 16 + 1023) & ~1023u;
+  static constexpr uint32_t kStageBytes = 4 * 2 * 2048;
+  static constexpr uint32_t kTotal = kStageOff + kStageBytes;
   static constexpr uint32_t kAlloc = kTotal + 1024;              // slack for 1 KB alignment
 };
 
@@ -151,6 +155,7 @@ struct SmemAnyK {
   static constexpr uint32_t kBarOff = 2 * kStage;
   static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kStageOff = 0, kStageBytes = 0;   // no TMA-store staging
   static constexpr uint32_t kTotal = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kTotal + 1024;
   // Transaction bytes of one stage's boxes.
@@ -178,10 +183,13 @@ template <> struct Smem<Fmt::kInt8> {
   static constexpr uint32_t kBarOff = kSOff;
   static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kStageOff = 0, kStageBytes = 0;   // no TMA-store staging
   static constexpr uint32_t kTotal = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
 static_assert(Smem<Fmt::kInt8>::kAlloc <= 232448, "W8A8 stages fit in shared memory");
+static_assert(Smem<Fmt::kFp8>::kAlloc <= 232448 && Smem<Fmt::kNvfp4>::kAlloc <= 232448,
+              "stages and output staging fit in shared memory");
 
 static_assert(UMMA_M * kPartStride <= Smem<Fmt::kInt8>::kBarOff &&
               UMMA_M * kPartStride <= Smem<Fmt::kNvfp4>::kBarOff &&
@@ -203,6 +211,7 @@ struct Problem {
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
   int a_groups, w_groups;      // any-K path: full 8-row groups of A, 16-row groups of W
+  int tma_out;                 // 16-bit output stored through the output tensor map
   Epi ep;                      // output type and fused epilogue
   const float* a_scale;        // W8A8: per-row scale of A [M]
   const float* b_scale;        // W8A8: per-output-column scale of W [N]
@@ -348,8 +357,8 @@ __device__ __forceinline__ void prefetch_span_l2(const uint8_t* base, int64_t lo
 template <Fmt F, bool kGrouped, bool kAnyK>
 __global__ void __launch_bounds__(kThreads, 1)
 k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-          const __grid_constant__ CUtensorMap tmap_x, const uint8_t* __restrict__ scales_g,
-          Problem p) {
+          const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_o,
+          const uint8_t* __restrict__ scales_g, Problem p) {
   using L = SmemFor<F, kAnyK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -824,6 +833,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // --------------------------------------------------------- epilogue --
     const int g = warp & 3;                 // TMEM lane group of this warp
     int it = 0;
+    const uint32_t stage = smem_base + L::kStageOff + g * 4096;   // this warp's 2 staging boxes
+    int sbuf = 0;
     for (int t = t_first; t < total_tiles; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid) continue;
@@ -904,6 +915,42 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             for (int i = 0; i < 32; ++i)
               v[i] = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), sa), __shfl_sync(0xFFFFFFFFu, sbv, i));
           }
+          // TMA store of the warp's 32 x 32 box (16-bit outputs, all rows of
+          // the box inside the tile or, for the plain GEMM, past the end of
+          // the output where the store clips them): every lane stages its row.
+          const int mbox = tl.m0 + h * UMMA_M + g * 32;
+          const bool use_box = L::kStageBytes > 0 && !kAnyK && p.tma_out && n < p.N &&
+                               mbox < tl.m_end && (!kGrouped || mbox + 32 <= tl.m_end);
+          if (use_box) {
+            const int lim = min(32, p.N - n);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = tl.scale * __uint_as_float(r[i]);
+            if (!plain_epi) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = epi_apply(p.ep, v[i], bias0 + n + (i < lim ? i : 0));
+            }
+            const uint32_t buf = stage + sbuf * 2048;
+            if (lane == 0) tc::bulk_wait_read<1>();   // the store from this buffer two boxes ago has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                w4[q] = p.ep.out_kind == kOutBf16 ? pack_bf16x2(v[8 * j + 2 * q], v[8 * j + 2 * q + 1])
+                                                  : pack_f16x2(v[8 * j + 2 * q], v[8 * j + 2 * q + 1]);
+              tc::sts128(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4),
+                         make_uint4(w4[0], w4[1], w4[2], w4[3]));
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tc::tma_store_2d(&tmap_o, buf, n, mbox);
+              tc::bulk_commit();
+            }
+            sbuf ^= 1;
+            continue;
+          }
           if (!row_ok || n >= p.N) continue;
           const int lim = min(32, p.N - n);
           if constexpr (F != Fmt::kInt8) {
@@ -944,6 +991,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
     }
+    // Every TMA store of this warp has completed before the CTA exits.
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
   }
 
   tc::tc_fence_before();
@@ -1004,7 +1054,8 @@ __global__ void k_fill_scaled_zero(void* out, Epi ep, int64_t count, int64_t N, 
 
 template <Fmt F, bool kGrouped, bool kAnyK = false>
 cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, const uint8_t* scales,
-                   const Problem& p, int grid, const CUtensorMap* tx = nullptr) {
+                   const Problem& p, int grid, const CUtensorMap* tx = nullptr,
+                   const CUtensorMap* to = nullptr) {
   auto kern = k_wq_gemm<F, kGrouped, kAnyK>;
   const uint32_t smem = SmemFor<F, kAnyK>::kAlloc;
   // The shared-memory opt-in is set once per device (it is not a stream
@@ -1030,13 +1081,23 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   cfg.numAttrs = p.ksplit > 1 ? 1 : 0;
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, scales, p);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, to ? *to : unused, scales, p);
 }
 
 cudaError_t fill_zero(const Ctx& c, void* out, const Epi& ep, int64_t count, int64_t N, float alpha) {
   const int grid = static_cast<int>(std::min<int64_t>((count + 255) / 256, c.num_sms * 8LL));
   k_fill_scaled_zero<<<grid > 0 ? grid : 1, 256, 0, c.stream>>>(out, ep, count, N > 0 ? N : 1, alpha);
   return cudaGetLastError();
+}
+
+// The output tensor map for TMA stores of the epilogue's 32 x 32 boxes:
+// 16-bit outputs whose rows are 16-byte strided (N % 8 == 0).  Returns
+// whether it was made (1) or the epilogue stores directly (0).
+int output_map(const Epi& ep, void* out, int64_t rows, int64_t N, CUtensorMap* to) {
+  memset(to, 0, sizeof(*to));
+  if (ep.out_kind == kOutF32 || N % 8 != 0 || rows <= 0 || N <= 0) return 0;
+  const auto dt = ep.out_kind == kOutBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return encode_2d(to, dt, out, N, rows, N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
 }
 
 Problem base_problem(const Ctx& c, void* out, const Epi& ep, int64_t M, int64_t N, int64_t K,
@@ -1112,7 +1173,9 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
   Problem p = base_problem(c, out, ep, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
   const int grid = plan_split(c, p, tiles);
-  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, grid);
+  CUtensorMap to;
+  p.tma_out = output_map(ep, out, M, N, &to);
+  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, grid, nullptr, &to);
 }
 
 cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
@@ -1130,7 +1193,9 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void
   Problem p = base_problem(c, out, ep, M, N, K, alpha);
   const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
   const int grid = plan_split(c, p, tiles);
-  return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid);
+  CUtensorMap to;
+  p.tma_out = output_map(ep, out, M, N, &to);
+  return launch<Fmt::kNvfp4, false>(c, ta, tw, bs, p, grid, nullptr, &to);
 }
 
 cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_t* a,
@@ -1188,9 +1253,11 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep, cons
       return cudaErrorInvalidValue;
   }
   int grid = 1;
-  const Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
-                                    max_rows, total_M, N, K, &grid);
-  return launch<Fmt::kFp8, true>(c, ta, tw, nullptr, p, grid);
+  Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
+                              max_rows, total_M, N, K, &grid);
+  CUtensorMap to;
+  p.tma_out = output_map(ep, out, total_M, N, &to);
+  return launch<Fmt::kFp8, true>(c, ta, tw, nullptr, p, grid, nullptr, &to);
 }
 
 cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
@@ -1210,9 +1277,11 @@ cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep, co
       return cudaErrorInvalidValue;
   }
   int grid = 1;
-  const Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
-                                    max_rows, total_M, N, K, &grid);
-  return launch<Fmt::kNvfp4, true>(c, ta, tw, bs, p, grid);
+  Problem p = grouped_problem(c, out, ep, a_offsets, expert_ids, expert_scales, G, E,
+                              max_rows, total_M, N, K, &grid);
+  CUtensorMap to;
+  p.tma_out = output_map(ep, out, total_M, N, &to);
+  return launch<Fmt::kNvfp4, true>(c, ta, tw, bs, p, grid, nullptr, &to);
 }
 
 }  // namespace gq

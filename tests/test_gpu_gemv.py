@@ -230,3 +230,36 @@ def test_launch_flags_reject_unknown_bits():
     lib()
     with pytest.raises(gq.GQError):
         gq.set_launch_flags(0x80)
+
+
+def test_overlap_flag_orders_few_row_gemm(overlap_flag):
+    """The few-row GEMM with the overlap flag: a chain of dependent products
+    (each output, 16 x 512, is the next input) and a torch kernel writing
+    the activations right before one; every activation read and output write
+    stays ordered after the previous kernel."""
+    m, n = 16, 512
+    qs = [synth.nvfp4_weight(n, n, seed=50 + i) for i in range(3)]
+    dq = [(q.to(DEV), bs.to(DEV)) for q, bs, _ in qs]
+    a0 = synth.bf16_activations(m, n, seed=60)
+    a = a0.to(DEV)
+    outs = []
+    for i in range(3):
+        c = gq.nvfp4_matmul(a, dq[i][0], dq[i][1], qs[i][2], out_dtype=torch.bfloat16)
+        outs.append(c)
+        a = c
+    at = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    at.copy_(a0.to(DEV))
+    ct = gq.nvfp4_matmul(at, dq[0][0], dq[0][1], qs[0][2], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ain = bits(a0)
+    for i in range(3):
+        q, bs, s2 = qs[i]
+        w_hat = oracle.decode_nvfp4(q.numpy(), bs.numpy())
+        ref = oracle.nvfp4_matmul(ain, q.numpy(), bs.numpy(), s2)
+        assert_within(to_f64(outs[i]), ref, oracle.tolerance(ain, w_hat, s2, True, ref=ref),
+                      f"chain step {i}")
+        ain = bits(outs[i].cpu())
+    q, bs, s2 = qs[0]
+    ref = oracle.nvfp4_matmul(bits(a0), q.numpy(), bs.numpy(), s2)
+    assert_within(to_f64(ct), ref, oracle.tolerance(bits(a0), oracle.decode_nvfp4(q.numpy(), bs.numpy()), s2),
+                  "after torch write")
