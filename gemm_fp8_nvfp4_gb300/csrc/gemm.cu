@@ -1,5 +1,6 @@
-// gemm.cu -- W8A16 / W4A16 GEMMs and the grouped (MoE) W8A16 GEMM on the
-// 5th-generation tensor cores (tcgen05) of sm_103a.
+// gemm.cu -- W8A16 / W4A16 GEMMs, the grouped (MoE) GEMMs of both formats
+// and the W8A8 int8 GEMM on the 5th-generation tensor cores (tcgen05) of
+// sm_103a.
 //
 //   C[m, n] = alpha * sum_k A[m, k] * w_hat[n, k]      (A bf16, fp32 accumulate)
 //
@@ -31,7 +32,14 @@
 //                 256-column fp32 accumulators fill TMEM; stages are released
 //                 with tcgen05.commit.
 //   warps 12..15  epilogue: tcgen05.ld both accumulators, multiply by the
-//                 scale, convert (RNE) and store with bounds guards.
+//                 scale, apply the fused epilogue, convert (RNE) and store:
+//                 16-bit outputs as 32 x 32 boxes staged in shared memory and
+//                 written by TMA (TMEM is free again before the stores land),
+//                 otherwise directly with bounds guards.
+//   warps 2, 3    idle.
+// W8A8 (Fmt::kInt8): the A tile is int8 too; the dequant warps widen both
+// operands exactly to binary16 (MMA kind::f16 with f16 inputs) and the
+// epilogue multiplies by a_scale[m] and b_scale[n].
 // Tiles are visited m-fastest so that consecutive CTAs share a weight tile
 // through L2 (the pages' Morton raster serves the same purpose).
 //
