@@ -162,3 +162,18 @@ def test_nvfp4_grouped_rejects_bad_k():
     st = l.gq_nvfp4_grouped_matmul(c.data_ptr(), 0, a.data_ptr(), w.data_ptr(), w.data_ptr(),
                                    o.data_ptr(), o.data_ptr(), None, 1, 1, 4, 4, 32, 96, None)
     assert st == 2  # GQ_ERR_SHAPE
+
+
+def test_nvfp4_grouped_k_zero_writes_zeros():
+    """K = 0: every covered row is an empty sum (zeros); uncovered rows stay."""
+    lib()
+    q = torch.zeros((2, 64, 0), dtype=torch.uint8, device=DEV)
+    bs = torch.zeros((2, 64, 0), dtype=torch.uint8, device=DEV)
+    a = torch.zeros((10, 0), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((10, 64), SENTINEL, dtype=torch.float32, device=DEV)
+    gq.nvfp4_grouped_matmul(a, q, bs, torch.tensor([1, 5, 9], dtype=torch.int32, device=DEV),
+                            torch.tensor([0, -1], dtype=torch.int32, device=DEV), None,
+                            max_rows_per_group=8, out=out)
+    got = out.cpu()
+    assert torch.all(got[1:9] == 0.0)
+    assert torch.all(got[0] == SENTINEL) and torch.all(got[9] == SENTINEL)

@@ -183,3 +183,13 @@ def test_quantize_exact_ties_and_tiny_rows():
     want_q, want_s = oracle.int8_quantize_rows(bits(x))
     assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
     assert np.array_equal(q.cpu().numpy(), want_q)
+
+
+def test_quantize_rows_k_zero_and_m_zero():
+    lib()
+    x = torch.zeros((3, 0), dtype=torch.bfloat16, device=DEV)
+    q, s = gq.int8_quantize_rows(x)
+    assert q.shape == (3, 0) and torch.equal(s.cpu(), torch.zeros(3))
+    x = torch.zeros((0, 32), dtype=torch.bfloat16, device=DEV)
+    q, s = gq.int8_quantize_rows(x)
+    assert q.shape == (0, 32) and s.numel() == 0
