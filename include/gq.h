@@ -15,6 +15,9 @@
  *            elements of a row; the per-tensor second scale (weight_scale_2)
  *            is passed as `alpha`.  Source: the "fp4_matmul" kernel page
  *            (kernels/linalg/matmul/gpu/apple/fp4_matmul), first paragraph.
+ * And the W8A8 int8 sibling method of the "int8_matmul" page
+ * (gq_int8_quantize_rows, gq_int8_matmul): int8 activations and weights with
+ * per-row and per-column scales.
  *
  * Common conventions for every entry point below
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
