@@ -53,7 +53,9 @@
 // warps then shift each row by its fixed misalignment, zero the K tail, and
 // write A and the decoded weight in the swizzled layout.  A's rows are
 // realigned in place and kept in residue order (tile row 8 i + r at smem row
-// 32 r + i), which the epilogue undoes when it picks the output row.
+// 32 r + i), which the epilogue undoes when it picks the output row.  When
+// K % 8 == 0, A's rows are 16-byte strided and A comes as the plain tiled
+// box of the main path instead (normal row order, no realignment).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -220,6 +222,7 @@ struct Problem {
   int G, E, max_rows;          // grouped only
   int a_groups, w_groups;      // any-K path: full 8-row groups of A, 16-row groups of W
   int tma_out;                 // 16-bit output stored through the output tensor map
+  int a_tma;                   // any-K path with K % 8 == 0: A by the plain tiled map
   Epi ep;                      // output type and fused epilogue
   const float* a_scale;        // W8A8: per-row scale of A [M]
   const float* b_scale;        // W8A8: per-output-column scale of W [N]
@@ -417,6 +420,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     tc::tma_prefetch_desc(&tmap_w);
   }
   if (kAnyK && warp == kWarpTma && lane == 0) {
+    if (p.a_tma) tc::tma_prefetch_desc(&tmap_a);
     if (p.a_groups > 0) {
       tc::tma_prefetch_desc(&tmap_a);
       tc::tma_prefetch_desc(&tmap_x);
@@ -538,7 +542,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       tc::cp_async_16(dst, n ? src : any, n);
     };
     constexpr uint32_t kTx0 = SmemAnyK::kABoxBytes, kTx1 = SmemAnyK::kWBoxBytes;
-    const uint32_t tx = (p.a_groups > 0 ? kTx0 : 0u) + (p.w_groups > 0 ? kTx1 : 0u);
+    // K % 8 == 0: A's rows are 16-byte strided and come as one plain tiled
+    // box per stage (128-byte swizzle, the MMA's layout); only W needs the
+    // residue boxes.
+    const uint32_t tx = (p.a_tma ? kABytes : p.a_groups > 0 ? kTx0 : 0u) + (p.w_groups > 0 ? kTx1 : 0u);
     prefetch_tile(t_first);
     int s = 0;
     uint32_t ph = 0;
@@ -547,7 +554,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const Tile tl = get_tile<kGrouped>(p, t);
       prefetch_tile(t + t_step);
       if (!tl.valid || tl.expert < 0) continue;
-      const bool a_part = tl.m_end > a_full;
+      const bool a_part = !p.a_tma && tl.m_end > a_full;
       const bool w_part = min(tl.n0 + BN, p.N) > w_full;
       for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
@@ -558,7 +565,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         uint8_t* st = smem + s * SmemAnyK::kStage;
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(&full_raw[s], tx);
-          if (p.a_groups > 0) {
+          if (p.a_tma) {
+            tc::tma_load_2d(st, &tmap_a, &full_raw[s], static_cast<int>(k0), tl.m0);
+          } else if (p.a_groups > 0) {
             const int g0 = tl.m0 / 8;
 #pragma unroll 1
             for (int r = 0; r < 8; ++r) {
@@ -624,7 +633,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const uint32_t acc_ph = it & 1;
       ++it;
       // (Any K: the rows are in residue order, spread over both halves.)
-      const bool two_halves = kAnyK || tl.m_end - tl.m0 > UMMA_M;
+      const bool two_halves = (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > UMMA_M;
       // Both accumulators free (the epilogue of the previous tile has read them).
       if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
@@ -706,7 +715,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         const int kv = min(BK, p.K - kb * BK);     // valid K of this stage, >= 1
         const uint32_t st = smem_base + s * SmemAnyK::kStage;
-        {
+        if (!p.a_tma) {
           uint32_t out[32];
           if (a_act) {
             uint32_t in[36];
@@ -898,12 +907,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const bool plain_epi = epi_plain(p.ep);
       const bool vec_ok = p.ep.out_kind == kOutF32 ? (p.N % 4 == 0) : (p.N % 8 == 0);
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
-      const int halves = (kAnyK || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
+      const bool residue_rows = kAnyK && !p.a_tma;
+      const int halves = (residue_rows || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
         // TMEM lane h * 128 + 32 g + lane holds tile row h * 128 + 32 g + lane,
         // or (any K, residue order) tile row 8 lane + 4 h + g.
-        const int m = kAnyK ? tl.m0 + 8 * lane + 4 * h + g : tl.m0 + h * UMMA_M + g * 32 + lane;
+        const int m = residue_rows ? tl.m0 + 8 * lane + 4 * h + g : tl.m0 + h * UMMA_M + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
 #pragma unroll 1
@@ -1157,8 +1167,12 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
     Problem p = base_problem(c, out, ep, M, N, K, alpha);
     p.a_g = a;
     p.w_g = w;
-    p.a_groups = static_cast<int>(M / 8);
+    p.a_tma = K % 8 == 0 ? 1 : 0;
+    p.a_groups = p.a_tma ? 0 : static_cast<int>(M / 8);
     p.w_groups = static_cast<int>(N / 16);
+    if (p.a_tma && !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
     if (p.a_groups > 0 &&
         (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72, kAnyInTile,
                     CU_TENSOR_MAP_SWIZZLE_NONE) ||

@@ -1,8 +1,9 @@
-"""FP8 GEMM with K not a multiple of 16: the plain-load producer path.
+"""FP8 GEMM with K not a multiple of 16: the residue-class staging path.
 
-Rows of A (2K bytes) and W (K bytes) are then not 16-byte strided, so the
-operands are read with aligned 4-byte loads and realigned in registers; the
-K tail of the last stage is zero.  Same tolerance as the aligned GEMM:
+Rows of A (2K bytes) and W (K bytes) are then not 16-byte strided: rows 8
+(A) and 16 (W) apart are, so one TMA box per residue class brings the
+16-byte-aligned windows that are realigned in shared memory (A by a plain
+tiled box when K % 8 == 0); the K tail of the last stage is zero.  Same tolerance as the aligned GEMM:
 |gpu - oracle| <= 2e-4 * |alpha| * sum_k |a_k w_k| (+1 ulp of the output type).
 """
 
@@ -49,7 +50,8 @@ def check(m, n, k, out_dtype=torch.float32, seed=0, rows=None, bias=None, act="n
 
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1), (3, 5, 7), (17, 33, 3), (200, 384, 520),
                                    (130, 257, 65), (257, 300, 129), (513, 700, 1001),
-                                   (64, 4096, 4099), (300, 1000, 4100), (129, 520, 2)])
+                                   (64, 4096, 4099), (300, 1000, 4100), (129, 520, 2),
+                                   (513, 700, 1000), (7, 40, 8), (260, 300, 24), (128, 256, 4104)])
 def test_anyk_shapes(m, n, k):
     lib()
     check(m, n, k, seed=m + n + k)
@@ -67,13 +69,14 @@ def test_anyk_epilogue():
     check(260, 448, 333, torch.bfloat16, seed=8, bias=bias, act="silu")
 
 
-def test_anyk_prefill_sampled():
-    """M=2048, N=14336 with K=4100 (the prefill shape with a ragged K);
-    the oracle checks sampled rows."""
+@pytest.mark.parametrize("k", [4100, 4104])
+def test_anyk_prefill_sampled(k):
+    """M=2048, N=14336 with K=4100 and 4104 (the prefill shape with a ragged
+    K; 4104 takes the plain A box); the oracle checks sampled rows."""
     lib()
     rng = np.random.default_rng(1)
     rows = sorted(set([0, 1, 127, 128, 255, 2047] + list(rng.integers(0, 2048, 30))))
-    check(2048, 14336, 4100, torch.bfloat16, seed=3, rows=rows)
+    check(2048, 14336, k, torch.bfloat16, seed=3, rows=rows)
 
 
 def test_anyk_identity_every_code():
