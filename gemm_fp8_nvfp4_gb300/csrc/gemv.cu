@@ -10,13 +10,14 @@
 // layout of the "fp4_matmul" page.
 //
 // GB300 design.  The kernel is HBM-bound: every weight byte is read exactly
-// once and nothing else is large.  A CTA of 8 warps owns R consecutive rows
-// and splits K across all 256 threads (thread t takes vectors t, t+256, ...),
-// so each thread streams R rows x U vectors of 16-byte weight loads before it
-// does any arithmetic (deep memory-level parallelism: ~32 KB in flight per
-// CTA), and the bf16 activation chunk it loads once is reused for all R rows.
-// The R partial sums are reduced with xor-shuffles inside each warp and then
-// across the 8 warps in a fixed order through shared memory (deterministic).
+// once and nothing else is large.  A CTA of 4 warps owns R = 4 consecutive
+// rows and splits K across its 128 threads (thread t takes vectors t, t+128,
+// ...), so each thread streams R rows x up to U vectors of 16-byte weight
+// loads before it does any arithmetic (deep memory-level parallelism: up to
+// 32 KB in flight per CTA), and the bf16 activation chunk it loads once is
+// reused for all R rows.  The R partial sums are reduced with xor-shuffles
+// inside each warp and then across the 4 warps in a fixed order through
+// shared memory (deterministic).
 // Weight loads bypass L1 (read once); activation loads go through L1 because
 // every CTA on the SM reads the same x.
 //
@@ -41,7 +42,7 @@
 namespace gq {
 namespace {
 
-constexpr int kThreads = 128;   // threads per CTA (8 CTAs fit on an SM)
+constexpr int kThreads = 128;   // threads per CTA
 
 // ---------------------------------------------------------------- helpers --
 

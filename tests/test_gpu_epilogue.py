@@ -49,7 +49,7 @@ def expected(pre, ab, w_hat, alpha, bias_f64, act, out_dtype):
 
 
 @pytest.mark.parametrize("act,bias_dtype,out_dtype", CASES)
-@pytest.mark.parametrize("n,k", [(1000, 4096), (1003, 520)])
+@pytest.mark.parametrize("n,k", [(1000, 4096), (1003, 520), (2000, 4096)])
 def test_fp8_gemv_epilogue(act, bias_dtype, out_dtype, n, k):
     lib()
     codes, scale = synth.fp8_weight(n, k, seed=n + k)

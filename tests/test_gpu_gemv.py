@@ -170,6 +170,18 @@ def test_gemv_row_splits(n, k):
         run_nvfp4(n, k, torch.float32, seed=n + 1)
 
 
+@pytest.mark.parametrize("n,k", [(1216, 16), (1217, 4112), (2000, 16384), (1500, 12304),
+                                 (3000, 8192), (3653, 1024), (20000, 256)])
+def test_fp8_gemv_large_n(n, k):
+    """Many rows per SM with 16-byte vectors: one vector per row (K = 16),
+    threads with one to several vectors per row and a remainder past the
+    unrolled batches (K = 4112, 12304), long rows (K = 16384) and a row count
+    that leaves the last CTA ragged."""
+    lib()
+    run_fp8(n, k, torch.float32, seed=n + k)
+    run_fp8(n, k, torch.bfloat16, seed=n + k + 1)
+
+
 @pytest.fixture
 def overlap_flag():
     """GQ_LAUNCH_OVERLAP_WEIGHT_READS on for the test, restored afterwards."""
@@ -180,8 +192,9 @@ def overlap_flag():
     gq.set_launch_flags(old)
 
 
-def test_overlap_flag_gives_identical_results(overlap_flag):
-    codes, scale = synth.fp8_weight(1000, 4096, seed=21)
+@pytest.mark.parametrize("n8", [1000, 3000])
+def test_overlap_flag_gives_identical_results(overlap_flag, n8):
+    codes, scale = synth.fp8_weight(n8, 4096, seed=21)
     q, bs, s2 = synth.nvfp4_weight(1000, 4096, seed=22)
     x = synth.bf16_activations(1, 4096, seed=23).reshape(-1).to(DEV)
     w, qd, bsd = codes.to(DEV), q.to(DEV), bs.to(DEV)
