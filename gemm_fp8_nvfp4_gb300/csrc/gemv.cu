@@ -26,7 +26,8 @@
 // griddepcontrol.launch_dependents at its start: its CTAs become resident
 // while the previous kernel finishes and wait (griddepcontrol.wait) before
 // touching global memory, so stream order is kept and the launch gap between
-// back-to-back GEMVs is hidden.  With GQ_LAUNCH_OVERLAP_WEIGHT_READS each
+// back-to-back GEMVs is hidden; before that wait they prefetch their first
+// weight bytes into L2 (a prefetch returns no data, so order is unaffected).  With GQ_LAUNCH_OVERLAP_WEIGHT_READS each
 // thread issues its first batch of weight loads before that wait, and reads
 // x and writes y only after it: the weight stream of one GEMV overlaps the
 // tail of the previous kernel -- valid only when that kernel does not write
@@ -38,11 +39,31 @@
 // vector).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace gq {
 namespace {
 
 constexpr int kThreads = 128;   // threads per CTA
+// Weight prefetch before the wait for the previous kernel.  A prefetch
+// returns no data, so it may be issued while that kernel still runs: the
+// CTA's first weight bytes start moving from HBM into L2 during its tail and
+// the loads after the wait find them there.  FP8: the CTA's rows in one
+// prefetch when they total at most kPrefetchCtaBytes, else the first
+// kPrefetchRowHead bytes of each row (prefetching whole long rows competes
+// with the loads: 4096 x 14336 took 13.7 us instead of 10.1 us).  NVFP4: the
+// CTA's codes and block scales, one prefetch each (at most kPrefetchMax).
+constexpr int64_t kPrefetchCtaBytes = 16384;
+constexpr int64_t kPrefetchRowHead = 2048;
+constexpr int64_t kPrefetchMax = 65536;
+
+// L2 prefetch of the 16-byte-aligned part of [p, p + min(bytes, cap)).
+__device__ __forceinline__ void prefetch_l2(const uint8_t* p, int64_t bytes, int64_t cap) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(min(bytes, cap))) &
+                      ~static_cast<uintptr_t>(15);
+  if (e > a) tc::bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+}
 
 // ---------------------------------------------------------------- helpers --
 
@@ -178,7 +199,15 @@ k_fp8_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
   // waits after its first batch of weight loads.  Every GEMV lets the next
   // kernel's CTAs launch early too.
   pdl_launch_dependents();
-  if constexpr (!kOverlap || VEC != 16) pdl_wait();
+  if constexpr (!kOverlap || VEC != 16) {
+    const int64_t rows = row0 + R <= N ? R : N - row0;
+    if (rows * K <= kPrefetchCtaBytes) {
+      if (threadIdx.x == 0) prefetch_l2(w + row0 * K, rows * K, kPrefetchCtaBytes);
+    } else if (threadIdx.x < rows) {
+      prefetch_l2(w + (row0 + threadIdx.x) * K, K, kPrefetchRowHead);
+    }
+    pdl_wait();
+  }
   bool waited = !kOverlap || VEC != 16;
   constexpr int kWords = VEC >= 4 ? VEC / 4 : 1;
 
@@ -320,7 +349,14 @@ k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
   const int64_t half_k = K / 2;
   // Programmatic dependent launch as in k_fp8_gemv.
   pdl_launch_dependents();
-  if constexpr (!kOverlap) pdl_wait();
+  if constexpr (!kOverlap) {
+    if (threadIdx.x == 0) {
+      const int64_t rows = row0 + R <= N ? R : N - row0;
+      prefetch_l2(q + row0 * half_k, rows * half_k, kPrefetchMax);
+      prefetch_l2(bs + row0 * (K / 16), rows * (K / 16), kPrefetchMax);
+    }
+    pdl_wait();
+  }
   bool waited = !kOverlap;
   const int64_t nvec = half_k / VB;
   constexpr int kWords = VB / 4;
