@@ -110,9 +110,11 @@ typedef struct gq_epilogue {
  * and the few-row GEMM (gq_fp8_matmul / gq_nvfp4_matmul with M <= 128)
  * always launch their kernel as a programmatic dependent of the previous
  * kernel in the stream; by default every thread waits for that kernel to
- * finish (and its writes to become visible) before it touches any global
- * memory, so stream order is unchanged and only the launch gap (and, for the
- * GEMM, its set-up) is hidden.
+ * finish (and its writes to become visible) before it reads or writes any
+ * global memory, so stream order is unchanged and only the launch gap (and,
+ * for the GEMM, its set-up) is hidden.  Before that wait a GEMV CTA issues
+ * an L2 prefetch of its first weight bytes: a prefetch returns no data to
+ * the kernel (L2 is coherent), so it does not change what is read.
  *
  * GQ_LAUNCH_OVERLAP_WEIGHT_READS: each GEMV thread, and the few-row GEMM's
  * weight producer, issue their weight loads before that wait; activations
