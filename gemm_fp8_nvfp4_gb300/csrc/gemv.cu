@@ -25,13 +25,14 @@
 // in the stream (the programmatic stream serialization attribute) and calls
 // griddepcontrol.launch_dependents at its start: its CTAs become resident
 // while the previous kernel finishes and wait (griddepcontrol.wait) before
-// touching global memory, so stream order is kept and the launch gap between
-// back-to-back GEMVs is hidden; before that wait they prefetch their first
-// weight bytes into L2 (a prefetch returns no data, so order is unaffected).  With GQ_LAUNCH_OVERLAP_WEIGHT_READS each
-// thread issues its first batch of weight loads before that wait, and reads
-// x and writes y only after it: the weight stream of one GEMV overlaps the
-// tail of the previous kernel -- valid only when that kernel does not write
-// the weights, which is why it is opt-in.
+// reading or writing global memory, so stream order is kept and the launch
+// gap between back-to-back GEMVs is hidden; before that wait they prefetch
+// their first weight bytes into L2 (a prefetch returns no data, so what is
+// read is unaffected).  With GQ_LAUNCH_OVERLAP_WEIGHT_READS each thread
+// issues its first batch of weight loads before that wait, and reads x and
+// writes y only after it: the weight stream of one GEMV overlaps the tail of
+// the previous kernel -- valid only when that kernel does not write the
+// weights, which is why it is opt-in.
 //
 // The load width adapts to K and the pointers: 16 bytes when K % 16 == 0,
 // down to 1 byte for odd K (the pages' scalar tail for K % TILE_K != 0 becomes
@@ -45,6 +46,9 @@ namespace gq {
 namespace {
 
 constexpr int kThreads = 128;   // threads per CTA
+
+// ---------------------------------------------------------------- helpers --
+
 // Weight prefetch before the wait for the previous kernel.  A prefetch
 // returns no data, so it may be issued while that kernel still runs: the
 // CTA's first weight bytes start moving from HBM into L2 during its tail and
@@ -64,10 +68,6 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t* p, int64_t bytes, int
                       ~static_cast<uintptr_t>(15);
   if (e > a) tc::bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
 }
-
-// ---------------------------------------------------------------- helpers --
-
-
 // Load VEC bf16 activations starting at element k0 and widen to f32.
 template <int VEC>
 __device__ __forceinline__ void load_x(const uint16_t* __restrict__ x, int64_t k0, float* xf) {
@@ -191,19 +191,18 @@ k_fp8_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
   __shared__ float red[(T / 32) * R];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * R;
   const int64_t nvec = K / VEC;
-  // Overlap mode: the first batch of weight loads is issued before the wait
-  // for the previous kernel; x is read and y written only after it.
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: the CTAs become resident while that kernel finishes.  Plain
-  // order waits for it before touching any global memory; overlap mode
-  // waits after its first batch of weight loads.  Every GEMV lets the next
-  // kernel's CTAs launch early too.
+  // order prefetches the CTA's first weight bytes into L2, then waits for it
+  // before reading or writing global memory; overlap mode issues its first
+  // batch of weight loads before the wait (x is read and y written only
+  // after it).  Every GEMV lets the next kernel's CTAs launch early too.
   pdl_launch_dependents();
   if constexpr (!kOverlap || VEC != 16) {
-    const int64_t rows = row0 + R <= N ? R : N - row0;
-    if (rows * K <= kPrefetchCtaBytes) {
-      if (threadIdx.x == 0) prefetch_l2(w + row0 * K, rows * K, kPrefetchCtaBytes);
-    } else if (threadIdx.x < rows) {
+    const int64_t nrows = row0 + R <= N ? R : N - row0;
+    if (nrows * K <= kPrefetchCtaBytes) {
+      if (threadIdx.x == 0) prefetch_l2(w + row0 * K, nrows * K, kPrefetchCtaBytes);
+    } else if (threadIdx.x < nrows) {
       prefetch_l2(w + (row0 + threadIdx.x) * K, K, kPrefetchRowHead);
     }
     pdl_wait();
@@ -351,9 +350,9 @@ k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
   pdl_launch_dependents();
   if constexpr (!kOverlap) {
     if (threadIdx.x == 0) {
-      const int64_t rows = row0 + R <= N ? R : N - row0;
-      prefetch_l2(q + row0 * half_k, rows * half_k, kPrefetchMax);
-      prefetch_l2(bs + row0 * (K / 16), rows * (K / 16), kPrefetchMax);
+      const int64_t nrows = row0 + R <= N ? R : N - row0;
+      prefetch_l2(q + row0 * half_k, nrows * half_k, kPrefetchMax);
+      prefetch_l2(bs + row0 * (K / 16), nrows * (K / 16), kPrefetchMax);
     }
     pdl_wait();
   }
