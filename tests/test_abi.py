@@ -72,3 +72,35 @@ def test_product_package_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.replace("no oracle", ""), os.path.join(dirpath, f)
+
+
+def test_every_op_refuses_host_tensors():
+    """The product path has no CPU fallback: every op given host tensors
+    raises before anything runs (nothing is computed off the GPU)."""
+    import torch
+
+    import gemm_fp8_nvfp4_gb300 as gq
+
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    u8 = lambda *s: torch.zeros(*s, dtype=torch.uint8)
+    i8 = lambda *s: torch.zeros(*s, dtype=torch.int8)
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    i32 = lambda *s: torch.zeros(*s, dtype=torch.int32)
+    k = 64
+    calls = {
+        "fp8_gemv": lambda: gq.fp8_gemv(bf(k), u8(8, k), 1.0),
+        "nvfp4_gemv": lambda: gq.nvfp4_gemv(bf(k), u8(8, k // 2), u8(8, k // 16), 1.0),
+        "fp8_matmul": lambda: gq.fp8_matmul(bf(4, k), u8(8, k), 1.0),
+        "nvfp4_matmul": lambda: gq.nvfp4_matmul(bf(4, k), u8(8, k // 2), u8(8, k // 16), 1.0),
+        "fp8_grouped_matmul": lambda: gq.fp8_grouped_matmul(
+            bf(4, k), u8(2, 8, k), i32(3), i32(2), max_rows_per_group=4),
+        "nvfp4_grouped_matmul": lambda: gq.nvfp4_grouped_matmul(
+            bf(4, k), u8(2, 8, k // 2), u8(2, 8, k // 16), i32(3), i32(2), max_rows_per_group=4),
+        "int8_quantize_rows": lambda: gq.int8_quantize_rows(bf(4, k)),
+        "int8_matmul": lambda: gq.int8_matmul(i8(4, k), i8(8, k), f32(4), f32(8)),
+        "fp8_materialize": lambda: gq.fp8_materialize(u8(8, k)),
+        "nvfp4_materialize": lambda: gq.nvfp4_materialize(u8(8, k // 2), u8(8, k // 16)),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
