@@ -2,7 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or links
 this package: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
-leg of ``bench.py`` may use it.  It shares no code with the CUDA library.
+and reference (``--impl reference``) legs of ``bench.py`` may use it.  It
+shares no code with the CUDA library.
 
 It is the plain definition of what the method computes, written out in float64
 with numpy:
