@@ -239,6 +239,42 @@ def test_overlap_flag_orders_activation_reads(overlap_flag, n):
                   oracle.decode_fp8(codes[0].numpy()), 0.02)[0], "after torch write")
 
 
+@pytest.mark.parametrize("n,k", [(4096, 4096), (2048, 14336), (300, 1024)])
+def test_plain_order_sees_weights_written_just_before(n, k):
+    """Default launch flags: a torch kernel overwrites the weights right before
+    the GEMV.  The GEMV prefetches its first weight bytes into L2 before it
+    waits for that kernel; the values it reads must still be the new ones
+    (whole-CTA prefetch at K = 4096 and 1024, row heads at K = 14336)."""
+    lib()
+    assert gq.get_launch_flags() == 0
+    old8, scale = synth.fp8_weight(n, k, seed=70)
+    new8, _ = synth.fp8_weight(n, k, seed=71)
+    q_old, bs_old, s2 = synth.nvfp4_weight(n, k, seed=72)
+    q_new, bs_new, _ = synth.nvfp4_weight(n, k, seed=73)
+    x = synth.bf16_activations(1, k, seed=74).reshape(-1)
+    xd = x.to(DEV)
+    w = old8.to(DEV)
+    q, bs = q_old.to(DEV), bs_old.to(DEV)
+    new8_d, q_new_d, bs_new_d = new8.to(DEV), q_new.to(DEV), bs_new.to(DEV)
+    gq.fp8_gemv(xd, w, scale, out_dtype=torch.float32)      # old weights once through L2
+    gq.nvfp4_gemv(xd, q, bs, s2, out_dtype=torch.float32)
+    w.copy_(new8_d)
+    y8 = gq.fp8_gemv(xd, w, scale, out_dtype=torch.float32)
+    q.copy_(q_new_d)
+    bs.copy_(bs_new_d)
+    y4 = gq.nvfp4_gemv(xd, q, bs, s2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    xb = bits(x)
+    ref8 = oracle.fp8_gemv(xb, new8.numpy(), scale)
+    assert_within(to_f64(y8), ref8,
+                  oracle.tolerance(xb[None, :], oracle.decode_fp8(new8.numpy()), scale)[0],
+                  "fp8 after weight write")
+    ref4 = oracle.nvfp4_gemv(xb, q_new.numpy(), bs_new.numpy(), s2)
+    assert_within(to_f64(y4), ref4,
+                  oracle.tolerance(xb[None, :], oracle.decode_nvfp4(q_new.numpy(), bs_new.numpy()),
+                                   s2)[0], "nvfp4 after weight write")
+
+
 def test_launch_flags_reject_unknown_bits():
     lib()
     with pytest.raises(gq.GQError):
