@@ -172,11 +172,27 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ timing --
 
+# Set by our arm to gq.device_status: every timed region is followed by a read
+# of the library's status word, and a run in which any bounded in-kernel wait
+# gave up (the kernel then returns early with partial results) is an error,
+# never a figure.
+STATUS_CHECK = None
+
+
+def check_device_status(what: str):
+    if STATUS_CHECK is None:
+        return
+    st = STATUS_CHECK()
+    if st != 0:
+        raise RuntimeError(f"{what}: a kernel wait timed out (device status {st:#x}); "
+                           "the timing is invalid")
+
+
 def graph_timer(step_fn, steps, warmup, chunk, stream, world, sampler=None):
     """Run `warmup` eager steps, capture `chunk` steps into a CUDA graph and
     replay until exactly `steps` ran (the remainder as a second, shorter
     graph).  Returns the elapsed ms of the K timed steps (CUDA events on
-    `stream`)."""
+    `stream`); raises if a kernel reported a timed-out wait meanwhile."""
     with torch.cuda.stream(stream):
         for i in range(warmup):
             step_fn(i)
@@ -211,6 +227,7 @@ def graph_timer(step_fn, steps, warmup, chunk, stream, world, sampler=None):
     barrier(world)
     if sampler:
         sampler.stop()
+    check_device_status("timed region")
     return start.elapsed_time(end)
 
 
@@ -248,10 +265,12 @@ def nvfp4_bytes(m, n, k):
 
 def run_ours(args, rank, local, world):
     import gemm_fp8_nvfp4_gb300 as gq
+    global STATUS_CHECK
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     gq.load_library()
+    STATUS_CHECK = gq.device_status
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
     launches = {"n": 0}
@@ -339,6 +358,7 @@ def run_ours(args, rank, local, world):
         line["cpu_baseline"] = cpu_baseline_gemv(args)
         if not args.headline_only:
             line["cpu_baseline"]["per_config"] = cpu_baseline_configs()
+    line["device_status"] = gq.device_status()   # 0: no in-kernel wait gave up
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -397,6 +417,7 @@ def e2e_gemv(gq, base, dev, stream, args, world):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    check_device_status("end-to-end run")
     ms = e0.elapsed_time(e1)
     step_bytes = sum(fp8_gemv_bytes(n, k) for n, k in GEMV_SHAPES)
     total, ms_max = aggregate(world, step_bytes * steps, ms, device=dev)
@@ -778,9 +799,11 @@ def gemv_shape_times(gq, dev, stream, steps, warm):
 
 def run_only(args, local):
     import gemm_fp8_nvfp4_gb300 as gq
+    global STATUS_CHECK
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     gq.load_library()
+    STATUS_CHECK = gq.device_status
     stream = torch.cuda.Stream(device=dev)
     if args.overlap_weight_reads:
         gq.set_launch_flags(gq.GQ_LAUNCH_OVERLAP_WEIGHT_READS)

@@ -67,10 +67,12 @@ SIGNATURES = {
     "gq_nvfp4_materialize": (_I, [_P, _I, _P, _P, _I64, _I64, _P]),
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
     "gq_set_launch_flags": (_I, [ctypes.c_uint32]),
+    "gq_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "gq_get_launch_flags": (ctypes.c_uint32, []),
 }
 
 GQ_LAUNCH_OVERLAP_WEIGHT_READS = 1
+GQ_LAUNCH_TEST_STALL_PRODUCER = 2     # tests of the failure path only (include/gq.h)
 
 
 class GQError(RuntimeError):
@@ -116,8 +118,23 @@ def _check(status: int, where: str):
         raise GQError(status, where)
 
 
+def _current_device_index() -> int:
+    return torch.cuda.current_device()
+
+
+def _same_device(device: torch.device, name: str) -> None:
+    """The library launches on the current CUDA device and dereferences every
+    pointer there: a tensor or stream of another GPU is refused here, before
+    any launch, instead of reaching the kernels as a foreign address."""
+    cur = _current_device_index()
+    if device.type != "cuda" or device.index != cur:
+        raise ValueError(f"{name} is on {device} but the current device is cuda:{cur}; "
+                         "call torch.cuda.set_device() first")
+
+
 def _stream_handle(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
+    _same_device(torch.device(s.device), "stream")
     return s.cuda_stream
 
 
@@ -126,6 +143,7 @@ def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    _same_device(t.device, name)
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if ndim is not None and t.dim() != ndim:
@@ -427,6 +445,12 @@ def get_launch_flags() -> int:
     return int(load_library().gq_get_launch_flags())
 
 
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' bounded waits on the current device (0 = the
+    default 2 s); for tests of the failure path (synchronizes)."""
+    _check(load_library().gq_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
+
+
 def device_status(reset: bool = False) -> int:
     """Status flags recorded by bounded in-kernel waits that ran out (synchronizes)."""
     v = ctypes.c_uint32(0)
@@ -439,5 +463,6 @@ __all__ = [
     "nvfp4_grouped_matmul", "int8_quantize_rows", "int8_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
     "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
+    "GQ_LAUNCH_TEST_STALL_PRODUCER", "set_wait_limit_ns",
     "SIGNATURES", "LIB_PATH", "version", "status_str", "ACTIVATIONS", "Epilogue",
 ]

@@ -16,7 +16,14 @@
 
 namespace gq {
 
-__device__ uint32_t g_status_word;
+// Per-device record: the status word (bits of waits that ran out) and the
+// wait limit in ns that the kernels' bounded waits read (0 = the default).
+struct __align__(16) DeviceRecord {
+  uint32_t status;
+  uint32_t reserved;
+  uint64_t wait_limit_ns;
+};
+__device__ DeviceRecord g_device_record;
 
 namespace {
 
@@ -47,7 +54,7 @@ int device_ctx(cudaStream_t stream, Ctx* ctx) {
               cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
     void* status = nullptr;
     ok = ok && major == 10 && minor == 3;
-    ok = ok && cudaGetSymbolAddress(&status, g_status_word) == cudaSuccess;
+    ok = ok && cudaGetSymbolAddress(&status, g_device_record) == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       d.state.store(2, std::memory_order_release);
@@ -63,8 +70,9 @@ int device_ctx(cudaStream_t stream, Ctx* ctx) {
   ctx->status = d.status;
   ctx->num_sms = d.num_sms;
   ctx->device = dev;
-  ctx->overlap_weights =
-      (g_launch_flags.load(std::memory_order_relaxed) & GQ_LAUNCH_OVERLAP_WEIGHT_READS) != 0;
+  const uint32_t flags = g_launch_flags.load(std::memory_order_relaxed);
+  ctx->overlap_weights = (flags & GQ_LAUNCH_OVERLAP_WEIGHT_READS) != 0;
+  ctx->test_stall_producer = (flags & GQ_LAUNCH_TEST_STALL_PRODUCER) != 0;
   return GQ_OK;
 }
 
@@ -148,7 +156,8 @@ const char* gq_status_str(int s) {
 const char* gq_version(void) { return "gq 0.1.0 sm_103a"; }
 
 int gq_set_launch_flags(uint32_t flags) {
-  if (flags & ~static_cast<uint32_t>(GQ_LAUNCH_OVERLAP_WEIGHT_READS)) return GQ_ERR_SHAPE;
+  if (flags & ~static_cast<uint32_t>(GQ_LAUNCH_OVERLAP_WEIGHT_READS | GQ_LAUNCH_TEST_STALL_PRODUCER))
+    return GQ_ERR_SHAPE;
   gq::g_launch_flags.store(flags, std::memory_order_relaxed);
   return GQ_OK;
 }
@@ -339,7 +348,7 @@ int gq_int8_matmul_ex(void* c_out, int out_dtype, const int8_t* a, const int8_t*
   if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c_out, 16) || !aligned(a_scale, 4) ||
       !aligned(b_scale, 4))
     return GQ_ERR_ALIGN;
-  if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return GQ_ERR_TOO_LARGE;
+  if (M > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL || K > gq::kInt8MaxK) return GQ_ERR_TOO_LARGE;
   gq::Epi ep;
   if (int s = make_epi(out_dtype, epilogue, 0, &ep)) return s;
   gq::Ctx c;
@@ -377,6 +386,18 @@ int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q, const uint8
   if (int s = gq::device_ctx(stream, &c)) return s;
   const int kind = out_dtype == GQ_BF16 ? gq::kOutBf16 : (out_dtype == GQ_F16 ? gq::kOutF16 : gq::kOutF32);
   return gq::launch_status(gq::launch_nvfp4_materialize(c, out, kind, q, bs, N * K / 16));
+}
+
+int gq_set_wait_limit_ns(uint64_t ns) {
+  gq::Ctx c;
+  if (int s = gq::device_ctx(nullptr, &c)) return s;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(reinterpret_cast<uint8_t*>(c.status) + 8, &ns, sizeof(ns),
+                 cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return GQ_ERR_DEVICE;
+  }
+  return GQ_OK;
 }
 
 int gq_device_status(uint32_t* flags, int reset) {

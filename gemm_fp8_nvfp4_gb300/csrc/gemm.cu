@@ -37,9 +37,15 @@
 //                 written by TMA (TMEM is free again before the stores land),
 //                 otherwise directly with bounds guards.
 //   warps 2, 3    idle.
-// W8A8 (Fmt::kInt8): the A tile is int8 too; the dequant warps widen both
-// operands exactly to binary16 (MMA kind::f16 with f16 inputs) and the
-// epilogue multiplies by a_scale[m] and b_scale[n].
+// W8A8 (Fmt::kInt8): the A tile is int8 too and holds 128 rows.  The page's
+// int32 accumulation is kept exact on binary16 MMAs by splitting every A code
+// into two base-16 digits, a = 16 h + l (h in [-8, 8], l in [-8, 7]): the
+// dequant warps widen the weight codes and the two digit planes of A exactly
+// to binary16, the two MMA halves of the tile accumulate sum h*b and sum l*b
+// (each partial sum at most 1024 K in magnitude, so exact in float32 while K
+// per CTA <= 16320), and the epilogue forms the int32 sum 16 * H + L before
+// the dequant multiplies by a_scale[m] and b_scale[n].  Longer K is split
+// over a thread-block cluster whose int32 partials are added exactly.
 // Tiles are visited m-fastest so that consecutive CTAs share a weight tile
 // through L2 (the pages' Morton raster serves the same purpose).
 //
@@ -89,6 +95,11 @@ constexpr int kEpiWarp0 = 12;    // 4 warps: TMEM lane groups 0..3
 constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators (one per A half)
 
 constexpr uint32_t kPartStride = BN * 4 + 16;   // split-K partial row: 256 fp32 + pad
+// W8A8: K steps one CTA may sum (255 x 64 = 16320 K; every digit-plane partial
+// sum stays below 1024 x 16320 < 2^24, exact in float32).
+constexpr int kInt8MaxStepsPerCta = 255;
+static_assert(static_cast<int64_t>(kInt8MaxStepsPerCta) * BK * 8 == kInt8MaxK,
+              "the C ABI's W8A8 K limit is eight CTAs' worth");
 constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
 constexpr uint32_t kAHalfBytes = UMMA_M * BK * 2;  // 16 KB: offset of the second A half
 constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
@@ -176,12 +187,13 @@ struct SmemAnyK {
 template <Fmt F, bool kAnyK>
 using SmemFor = typename std::conditional<kAnyK, SmemAnyK, Smem<F>>::type;
 
-// W8A8: raw int8 A and W stages (16 KB each, 64-byte swizzle) and decoded
-// stages holding both operands as binary16 (W at +0, A at +32 KB).
+// W8A8: raw int8 A (8 KB, 128 rows) and W (16 KB) stages, 64-byte swizzle,
+// and decoded stages holding the weight and the two digit planes of A as
+// binary16 (W at +0, A's high digits at +32 KB, low digits at +48 KB).
 template <> struct Smem<Fmt::kInt8> {
   static constexpr int kRawSt = kRawStages;
   static constexpr int kDeqSt = kDeqStages;
-  static constexpr uint32_t kARawBytes = BM * BK;             // 16 KB of int8 A
+  static constexpr uint32_t kARawBytes = UMMA_M * BK;         // 8 KB: 128 rows of int8 A
   static constexpr uint32_t kAStride = kARawBytes;
   static constexpr bool kADeq = true;                         // MMA reads A from the decoded stage
   static constexpr uint32_t kDeqAOff = kDeqBytes;
@@ -217,6 +229,7 @@ struct Problem {
   uint32_t* status;
   float alpha;
   int M, N, K;                 // M = total rows for grouped
+  int bm;                      // A rows per tile of the plain GEMM (BM; W8A8: UMMA_M)
   int num_n_tiles;
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
@@ -230,6 +243,7 @@ struct Problem {
   const uint8_t* w_g;          // any-K path: W [N, K] e4m3 codes
   int ksplit;                  // > 1: split-K over a thread-block cluster of ksplit CTAs
   int kb_per_split;            // K steps per split
+  int stall_producer;          // GQ_LAUNCH_TEST_STALL_PRODUCER: the producer issues nothing
 };
 
 // A tile of work: rows [m0, m_end) of C, columns [n0, n0 + BN), weight index.
@@ -241,10 +255,10 @@ struct Tile {
 
 // Plain GEMM: tile t -> (m tile fastest, n tile).
 __device__ __forceinline__ Tile plain_tile(const Problem& p, int t) {
-  const int num_m = (p.M + BM - 1) / BM;
+  const int num_m = (p.M + p.bm - 1) / p.bm;
   Tile tl;
-  tl.m0 = (t % num_m) * BM;
-  tl.m_end = min(tl.m0 + BM, p.M);
+  tl.m0 = (t % num_m) * p.bm;
+  tl.m_end = min(tl.m0 + p.bm, p.M);
   tl.n0 = (t / num_m) * BN;
   tl.expert = 0;
   tl.scale = p.alpha;
@@ -253,7 +267,7 @@ __device__ __forceinline__ Tile plain_tile(const Problem& p, int t) {
 }
 
 __device__ __forceinline__ int plain_num_tiles(const Problem& p) {
-  return ((p.M + BM - 1) / BM) * p.num_n_tiles;
+  return ((p.M + p.bm - 1) / p.bm) * p.num_n_tiles;
 }
 
 // Grouped GEMM: the work list is every (group, m tile, n tile) whose group has
@@ -363,6 +377,13 @@ __device__ __forceinline__ void prefetch_span_l2(const uint8_t* base, int64_t lo
     tc::bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(kPiece, hi - o)));
 }
 
+// W8A8: the int32 sum 16 H + L from the float32 accumulators of the high and
+// low digit planes (both hold exact integers below 2^24, so the conversions
+// are exact; |16 H + L| <= 128 * 128 * K fits int32 for the K the host allows).
+__device__ __forceinline__ int digit_sum(uint32_t hi_bits, uint32_t lo_bits) {
+  return 16 * __float2int_rz(__uint_as_float(hi_bits)) + __float2int_rz(__uint_as_float(lo_bits));
+}
+
 // ----------------------------------------------------------------- kernel --
 
 template <Fmt F, bool kGrouped, bool kAnyK>
@@ -443,7 +464,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
 
-  if (warp == kWarpTma && !kAnyK) {
+  if (warp == kWarpTma && !kAnyK && p.stall_producer) {
+    // Failure-path test: no copy is issued, so every stage stays empty and
+    // the other roles' bounded waits run out (nothing asynchronous to drain).
+  } else if (warp == kWarpTma && !kAnyK) {
     // ------------------------------------------------------ TMA producer --
     int s = 0;
     uint32_t ph = 0;
@@ -633,7 +657,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const uint32_t acc_ph = it & 1;
       ++it;
       // (Any K: the rows are in residue order, spread over both halves.)
-      const bool two_halves = (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > UMMA_M;
+      // (W8A8: the halves are the two digit planes of the tile's 128 rows.)
+      const bool two_halves = F == Fmt::kInt8 || (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > UMMA_M;
       // Both accumulators free (the epilogue of the previous tile has read them).
       if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
@@ -790,12 +815,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
         if constexpr (F == Fmt::kInt8) {
           // Rows of 64 int8 codes (TMA 64-byte swizzle: chunk c at
-          // c ^ ((row >> 1) & 3)) -> binary16, exactly: the weight row, and
-          // the A row when the MMA reads it (a tile of at most 128 rows uses
-          // the first half only).
+          // c ^ ((row >> 1) & 3)) -> binary16, exactly: weight row `row`, and
+          // decoded A row `row` = digit row >> 7 (0: high, 1: low) of A row
+          // row & 127.
           const uint32_t a_raw = smem_base + L::kAOff + s * L::kAStride;
           const uint32_t a_dq = b_addr + L::kDeqAOff;
-          const bool do_a = row < UMMA_M || tl.m_end - tl.m0 > UMMA_M;
+          const int ar = row & (UMMA_M - 1);
+          const int digit = row >> 7;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint32_t src = row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
@@ -803,11 +829,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             s8x16_to_f16(tc::lds128(w_addr + src), lo, hi);
             tc::sts128(b_addr + sw128_off(row, 2 * c), lo);
             tc::sts128(b_addr + sw128_off(row, 2 * c + 1), hi);
-            if (do_a) {
-              s8x16_to_f16(tc::lds128(a_raw + src), lo, hi);
-              tc::sts128(a_dq + sw128_off(row, 2 * c), lo);
-              tc::sts128(a_dq + sw128_off(row, 2 * c + 1), hi);
-            }
+            const uint32_t asrc = ar * 64 + ((c ^ ((ar >> 1) & 3)) << 4);
+            s8x16_digit_to_f16(tc::lds128(a_raw + asrc), digit, lo, hi);
+            tc::sts128(a_dq + sw128_off(row, 2 * c), lo);
+            tc::sts128(a_dq + sw128_off(row, 2 * c + 1), hi);
           }
         } else if constexpr (F == Fmt::kFp8) {
           // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
@@ -886,6 +911,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         // padded to kPartStride bytes so that 8 consecutive rows hit
         // distinct banks.  The cluster reduction at the end of the kernel sums
         // the partials of all ranks.
+        // W8A8: the partial is the exact int32 sum 16 H + L of the two digit
+        // planes' accumulators (bits stored; the reduction adds int32).
         const int r_local = g * 32 + lane;
         const uint32_t prow = smem_base + r_local * kPartStride;
 #pragma unroll 1
@@ -893,6 +920,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + c0, r);
           tc::tmem_wait_ld();
+          if constexpr (F == Fmt::kInt8) {
+            uint32_t rl[32];
+            tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + BN + c0, rl);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(digit_sum(r[i], rl[i]));
+          }
           if (tl.m0 + r_local < tl.m_end) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -908,7 +942,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const bool vec_ok = p.ep.out_kind == kOutF32 ? (p.N % 4 == 0) : (p.N % 8 == 0);
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
       const bool residue_rows = kAnyK && !p.a_tma;
-      const int halves = (residue_rows || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
+      // W8A8: one half of output rows (the TMEM halves are its digit planes).
+      const int halves = F == Fmt::kInt8 ? 1 : (residue_rows || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
         // TMEM lane h * 128 + 32 g + lane holds tile row h * 128 + 32 g + lane,
@@ -924,14 +959,20 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           const int n = tl.n0 + c0;
           float v[32];
           if constexpr (F == Fmt::kInt8) {
-            // (acc * a_scale[m]) * b_scale[n], each product rounded once; lane
-            // i loads b_scale of column n + i and the warp shares it (every
-            // lane of the warp is here: the row test comes after).
+            // acc = 16 H + L exactly in int32 (the low-digit plane is the
+            // second TMEM half), then (float(acc) * a_scale[m]) * b_scale[n],
+            // each step rounded once; lane i loads b_scale of column n + i and
+            // the warp shares it (every lane of the warp is here: the row test
+            // comes after).
+            uint32_t rl[32];
+            tc::tmem_ld_32x32b_x32(taddr + BN + c0, rl);
+            tc::tmem_wait_ld();
             const float sbv = n + lane < p.N ? __ldg(p.b_scale + n + lane) : 0.f;
             const float sa = row_ok ? __ldg(p.a_scale + m) : 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              v[i] = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), sa), __shfl_sync(0xFFFFFFFFu, sbv, i));
+              v[i] = __fmul_rn(__fmul_rn(__int2float_rn(digit_sum(r[i], rl[i])), sa),
+                               __shfl_sync(0xFFFFFFFFu, sbv, i));
           }
           // TMA store of the warp's 32 x 32 box (16-bit outputs, all rows of
           // the box inside the tile or, for the plain GEMM, past the end of
@@ -1021,7 +1062,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // memory: rank r sums columns [r * BN / S, (r + 1) * BN / S) of the tile
     // over all ranks in rank order (deterministic), scales, converts, stores.
     tc::cluster_sync();
-    if (t_first < total_tiles) {
+    if (t_first < total_tiles && !*abort_flag) {   // an aborted CTA has no partial
       const Tile tl = get_tile<kGrouped>(p, t_first);
       const int rows = tl.m_end - tl.m0;
       const int cols = BN / p.ksplit;                 // multiple of 4 (host check)
@@ -1032,19 +1073,25 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const int c = c_begin + 4 * (task % (cols / 4));
         const uint32_t local = smem_base + r * kPartStride + c * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int iacc[4] = {0, 0, 0, 0};   // W8A8: exact int32 sums of the ranks' partials
         for (int q = 0; q < p.ksplit; ++q) {
           const float4 v = tc::ld_cluster_f4(tc::map_to_rank(local, q));
-          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          if constexpr (F == Fmt::kInt8) {
+            iacc[0] += __float_as_int(v.x); iacc[1] += __float_as_int(v.y);
+            iacc[2] += __float_as_int(v.z); iacc[3] += __float_as_int(v.w);
+          } else {
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
         }
         const int m = tl.m0 + r;
         const int n = tl.n0 + c;
         float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
         if constexpr (F == Fmt::kInt8) {
           const float sa = __ldg(p.a_scale + m);
-          const float in[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            o[i] = __fmul_rn(__fmul_rn(in[i], sa), __ldg(p.b_scale + min(n + i, p.N - 1)));
+            o[i] = __fmul_rn(__fmul_rn(__int2float_rn(iacc[i]), sa),
+                             __ldg(p.b_scale + min(n + i, p.N - 1)));
         }
         const int64_t base = static_cast<int64_t>(m) * p.N + n;
 #pragma unroll
@@ -1076,6 +1123,8 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
                    const CUtensorMap* to = nullptr) {
   auto kern = k_wq_gemm<F, kGrouped, kAnyK>;
   const uint32_t smem = SmemFor<F, kAnyK>::kAlloc;
+  Problem pl = p;
+  pl.stall_producer = (!kAnyK && c.test_stall_producer) ? 1 : 0;
   // The shared-memory opt-in is set once per device (it is not a stream
   // operation, so it is kept out of any CUDA-graph capture after the first call).
   static std::atomic<uint64_t> configured{0};
@@ -1099,7 +1148,7 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   cfg.numAttrs = p.ksplit > 1 ? 1 : 0;
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, to ? *to : unused, scales, p);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, to ? *to : unused, scales, pl);
 }
 
 cudaError_t fill_zero(const Ctx& c, void* out, const Epi& ep, int64_t count, int64_t N, float alpha) {
@@ -1127,6 +1176,7 @@ Problem base_problem(const Ctx& c, void* out, const Epi& ep, int64_t M, int64_t 
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
+  p.bm = BM;
   p.num_n_tiles = static_cast<int>((N + BN - 1) / BN);
   p.num_k_blocks = static_cast<int>((K + BK - 1) / BK);
   p.ep = ep;
@@ -1225,15 +1275,31 @@ cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_
                              int64_t M, int64_t N, int64_t K) {
   // K = 0: every sum is 0, so the output is the epilogue of 0.
   if (K == 0) return fill_zero(c, out, ep, M * N, N, 0.f);
+  if (K > kInt8MaxK) return cudaErrorInvalidValue;   // refused earlier by the C ABI
   CUtensorMap ta, tw;
-  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, UMMA_M, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   Problem p = base_problem(c, out, ep, M, N, K, 1.0f);
+  p.bm = UMMA_M;
   p.a_scale = a_scale;
   p.b_scale = b_scale;
-  const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
-  const int grid = plan_split(c, p, tiles);
+  const int tiles = ((p.M + UMMA_M - 1) / UMMA_M) * p.num_n_tiles;
+  int grid;
+  if (p.num_k_blocks <= kInt8MaxStepsPerCta) {
+    grid = plan_split(c, p, tiles);
+  } else {
+    // Each CTA's digit-plane sums stay exact only over at most
+    // kInt8MaxStepsPerCta K steps: split K over a cluster of 2, 4 or 8 CTAs
+    // (the column slices of the reduction need BN / S % 4 == 0), whose int32
+    // partials the cluster adds exactly.
+    int sp = 2;
+    while ((p.num_k_blocks + sp - 1) / sp > kInt8MaxStepsPerCta) sp *= 2;
+    if (sp > 8) return cudaErrorInvalidValue;
+    p.ksplit = sp;
+    p.kb_per_split = (p.num_k_blocks + sp - 1) / sp;
+    grid = tiles * sp;
+  }
   return launch<Fmt::kInt8, false>(c, ta, tw, nullptr, p, grid);
 }
 

@@ -25,10 +25,11 @@ struct Epi {
 // Per-call launch context filled by the C-ABI layer.
 struct Ctx {
   cudaStream_t stream;
-  uint32_t* status;   // device address of the per-device status word
+  uint32_t* status;   // device address of the per-device status word (then the wait limit)
   int num_sms;        // multiprocessor count of the current device
   int device;
   bool overlap_weights;  // GQ_LAUNCH_OVERLAP_WEIGHT_READS is set (gq_set_launch_flags)
+  bool test_stall_producer;  // GQ_LAUNCH_TEST_STALL_PRODUCER is set (tests only)
 };
 
 // Launch `kern` on c.stream.  With `pdl` the launch carries the programmatic
@@ -80,7 +81,9 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                     int64_t E, int64_t max_rows,
                                     int64_t total_M, int64_t N, int64_t K);
 
-// W8A8: c = epilogue((acc * a_scale[m]) * b_scale[n]), acc = sum a[m,k] b[n,k].
+// W8A8: c = epilogue((acc * a_scale[m]) * b_scale[n]), acc = sum a[m,k] b[n,k]
+// exactly in int32, for K <= kInt8MaxK (eight CTAs of 255 K steps of 64).
+constexpr int64_t kInt8MaxK = 130560;
 cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_t* a,
                              const int8_t* b, const float* a_scale, const float* b_scale,
                              int64_t M, int64_t N, int64_t K);

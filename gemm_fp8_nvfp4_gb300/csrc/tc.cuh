@@ -2,8 +2,9 @@
 // mbarriers, the tensor memory accelerator (TMA), cp.async, and the 5th-gen
 // tensor core (tcgen05: TMEM allocation, MMA, commit, TMEM loads).
 //
-// Every wait is bounded: it polls %globaltimer and, after kWaitLimitNs, records
-// a status bit in the device status word, raises a CTA-wide abort flag in
+// Every wait is bounded: it polls %globaltimer and, after the device's wait
+// limit (kWaitLimitNs unless gq_set_wait_limit_ns changed it), records a
+// status bit in the device status word, raises a CTA-wide abort flag in
 // shared memory and returns false, so the kernel can unwind instead of hanging.
 #pragma once
 
@@ -15,6 +16,14 @@ namespace gq {
 namespace tc {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// The per-device status word is the first 32-bit word of a 16-byte device
+// record whose bytes 8..15 hold the wait limit in ns (0 = kWaitLimitNs).
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* status) {
+  if (status == nullptr) return kWaitLimitNs;
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return v != 0 ? v : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -67,12 +76,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(a, parity)) return true;
+  const uint64_t limit = wait_limit_ns(status);
   const uint64_t t0 = globaltimer();
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       *abort = 1;
       record_status(status, bit);
       return false;

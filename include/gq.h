@@ -127,6 +127,17 @@ typedef struct gq_epilogue {
  * gq_set_launch_flags returns GQ_ERR_SHAPE for unknown bits.
  */
 #define GQ_LAUNCH_OVERLAP_WEIGHT_READS 1u
+/*
+ * GQ_LAUNCH_TEST_STALL_PRODUCER (tests only; never set it for real work):
+ * the tensor-core GEMM for M > 128 (FP8, NVFP4, W8A8 and grouped; not the
+ * few-row, any-K or GEMV kernels) launches with its copy producer idle, so
+ * no shared-memory stage ever fills, nothing asynchronous is issued, and every
+ * bounded wait of the kernel runs out: the call returns, the output is left
+ * unwritten, and gq_device_status reports the timed-out waits.  Use it with a
+ * short gq_set_wait_limit_ns to exercise that failure path without a fault.
+ * Not a citation of the pages.
+ */
+#define GQ_LAUNCH_TEST_STALL_PRODUCER 2u
 int gq_set_launch_flags(uint32_t flags);
 uint32_t gq_get_launch_flags(void);
 
@@ -292,14 +303,19 @@ int gq_int8_quantize_rows(int8_t* q, float* scale, const void* x, int64_t M, int
  *                 rounded once), then the epilogue (bias after the dequant,
  *                 activation), then the output conversion.
  *   c [M, N] (out_dtype), a [M, K] int8, b [N, K] int8 (one row per output
- *   column), a_scale [M], b_scale [N] float32.  K % 16 == 0.  a, b, c
- *   16-byte aligned; scales 4-byte aligned.
- * GB300 has no int8 tensor-core instruction on sm_103a (tcgen05 kind::i8
- * is not available there), so both operands are widened exactly to binary16
- * in shared memory and the sums are accumulated in float32: exact, and equal
- * to the int32 sums, while every |partial sum| stays below 2^24 (always when
- * sum_k |a[m,k] b[n,k]| < 2^24, e.g. K <= 1040); beyond that the sum is
- * rounded to float32 precision.
+ *   column), a_scale [M], b_scale [N] float32.  K % 16 == 0 and
+ *   K <= 130560 (GQ_ERR_TOO_LARGE beyond: |acc| then stays inside int32 for
+ *   any codes).  a, b, c 16-byte aligned; scales 4-byte aligned.
+ * acc is the exact int32 sum for every input, as on the page.  GB300 has no
+ * int8 tensor-core instruction on sm_103a (tcgen05 kind::i8 is not
+ * available there), so the sums run on binary16 tensor-core products: each
+ * code of a is split into two base-16 digits, a = 16 h + l with h in [-8, 8]
+ * and l in [-8, 7], the weight codes and both digit planes are widened
+ * exactly to binary16, the two float32 sums H = sum h b and L = sum l b are
+ * exact (every partial sum is an integer below 1024 K per CTA <= 2^24), and
+ * acc = 16 H + L is formed in int32.  K beyond 16320 is split over a
+ * thread-block cluster of 2, 4 or 8 CTAs whose int32 partials are added
+ * exactly.  acc is converted to float32 with round-to-nearest-even.
  */
 int gq_int8_matmul(void* c, int out_dtype, const int8_t* a, const int8_t* b,
                    const float* a_scale, const float* b_scale, int64_t M, int64_t N,
@@ -335,6 +351,17 @@ int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q,
  * non-zero the word is cleared afterwards.  Returns GQ_OK or GQ_ERR_DEVICE.
  */
 int gq_device_status(uint32_t* flags, int reset);
+
+/*
+ * How long a bounded in-kernel wait of the current device polls before it
+ * gives up (records its bit in the status word and lets the kernel unwind):
+ * `ns` nanoseconds, or the default of 2 s when ns == 0.  Applies to kernels
+ * launched after the call returns; synchronizes the device.  Meant for tests
+ * of the failure path (with GQ_LAUNCH_TEST_STALL_PRODUCER); a limit shorter
+ * than a kernel's real waits makes it give up on valid work.  Not a citation
+ * of the pages.  Returns GQ_OK or GQ_ERR_DEVICE.
+ */
+int gq_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }  /* extern "C" */

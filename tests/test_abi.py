@@ -104,3 +104,79 @@ def test_every_op_refuses_host_tensors():
     for name, call in calls.items():
         with pytest.raises(ValueError, match="CUDA tensor"):
             call()
+
+
+def test_every_op_refuses_tensors_of_another_device(monkeypatch):
+    """The library launches on the current device: operands, outputs and
+    streams of another GPU are refused in the binding before any launch.
+    Checked on the CPU with tensors that claim to live on cuda:1 while
+    cuda:0 is current (no GPU is touched)."""
+    import torch
+
+    import gemm_fp8_nvfp4_gb300 as gq
+
+    monkeypatch.setattr(gq, "_current_device_index", lambda: 0)
+
+    class OnCuda1(torch.Tensor):
+        @property
+        def is_cuda(self):
+            return True
+
+        @property
+        def device(self):
+            return torch.device("cuda", 1)
+
+    def far(t):
+        return torch.Tensor._make_subclass(OnCuda1, t)
+
+    bf = lambda *s: far(torch.zeros(*s, dtype=torch.bfloat16))
+    u8 = lambda *s: far(torch.zeros(*s, dtype=torch.uint8))
+    i8 = lambda *s: far(torch.zeros(*s, dtype=torch.int8))
+    f32 = lambda *s: far(torch.zeros(*s, dtype=torch.float32))
+    i32 = lambda *s: far(torch.zeros(*s, dtype=torch.int32))
+    k = 64
+    calls = {
+        "fp8_gemv": lambda: gq.fp8_gemv(bf(k), u8(8, k), 1.0),
+        "nvfp4_gemv": lambda: gq.nvfp4_gemv(bf(k), u8(8, k // 2), u8(8, k // 16), 1.0),
+        "fp8_matmul": lambda: gq.fp8_matmul(bf(4, k), u8(8, k), 1.0),
+        "nvfp4_matmul": lambda: gq.nvfp4_matmul(bf(4, k), u8(8, k // 2), u8(8, k // 16), 1.0),
+        "fp8_grouped_matmul": lambda: gq.fp8_grouped_matmul(
+            bf(4, k), u8(2, 8, k), i32(3), i32(2), max_rows_per_group=4),
+        "nvfp4_grouped_matmul": lambda: gq.nvfp4_grouped_matmul(
+            bf(4, k), u8(2, 8, k // 2), u8(2, 8, k // 16), i32(3), i32(2), max_rows_per_group=4),
+        "int8_quantize_rows": lambda: gq.int8_quantize_rows(bf(4, k)),
+        "int8_matmul": lambda: gq.int8_matmul(i8(4, k), i8(8, k), f32(4), f32(8)),
+        "fp8_materialize": lambda: gq.fp8_materialize(u8(8, k)),
+        "nvfp4_materialize": lambda: gq.nvfp4_materialize(u8(8, k // 2), u8(8, k // 16)),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="current device is cuda:0"):
+            call()
+
+    # a stream of another device is refused too; the current device passes
+    class FakeStream:
+        def __init__(self, index):
+            self.device = torch.device("cuda", index)
+            self.cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        gq._stream_handle(FakeStream(1))
+    assert gq._stream_handle(FakeStream(0)) == 0
+    gq._same_device(torch.device("cuda", 0), "x")
+
+
+def test_launch_flags_accept_the_test_stall_bit_only_as_declared(lib_path):
+    """gq_set_launch_flags takes GQ_LAUNCH_OVERLAP_WEIGHT_READS and
+    GQ_LAUNCH_TEST_STALL_PRODUCER (host state only, no GPU needed) and
+    refuses any other bit."""
+    import gemm_fp8_nvfp4_gb300 as gq
+    lib = gq.load_library(lib_path)
+    assert gq.GQ_LAUNCH_TEST_STALL_PRODUCER == 2
+    text = open(HEADER).read()
+    assert "#define GQ_LAUNCH_TEST_STALL_PRODUCER 2u" in text
+    try:
+        assert lib.gq_set_launch_flags(2) == 0 and lib.gq_get_launch_flags() == 2
+        assert lib.gq_set_launch_flags(3) == 0 and lib.gq_get_launch_flags() == 3
+        assert lib.gq_set_launch_flags(4) == 2 and lib.gq_get_launch_flags() == 3
+    finally:
+        assert lib.gq_set_launch_flags(0) == 0
