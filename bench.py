@@ -327,13 +327,30 @@ def run_ours(args, rank, local, world):
             "unit": "GB/s",
             "frac": round(value / world / peaks["hbm_gbs"], 4),
             "peak_source": peaks["source"],
-            "kernel": "k_fp8_gemv<16,4,4,128>",
+            "kernel": "k_fp8_gemv<16,4,U,128> (U = 2 for K = 4096, 4 for K = 14336)",
             "traffic": committed_traffic("fp8_gemv"),
             "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         },
         "gpu_launches": gemv_launches,
         "clocks": clocks,
     }
+
+    # The HBM floor of the same launches: each GEMV's kernel in its launch
+    # shape with the weight loads only (gq_probe_gemv_read_floor), same
+    # rotation, same replay.
+    def floor_step(i):
+        st = sets[i % copies]
+        for j, (w, s, x) in enumerate(st):
+            gq.probe_gemv_read_floor(w, out=outs[j], stream=stream)
+
+    ms_f = graph_timer(floor_step, args.steps, args.warmup, min(200, args.steps), stream, world)
+    _, ms_f = aggregate(world, step_bytes * args.steps, ms_f, device=dev)
+    line["roofline"]["floor"] = {
+        "what": "the same three launches with the loads only (gq_probe_gemv_read_floor)",
+        "ms_per_step": ms_f / args.steps,
+        "GB/s": round(step_bytes * args.steps / (ms_f * 1e-3) / 1e9, 1),
+        "frac": round(step_bytes * args.steps / (ms_f * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "value_over_floor": round(ms_f / ms_max, 4)}
 
     if not args.overlap_weight_reads and not args.headline_only:
         # The same step with GQ_LAUNCH_OVERLAP_WEIGHT_READS (decode with fixed
@@ -465,6 +482,16 @@ def nvfp4_subs(gq, dev, stream, peaks, world, steps, warm, subs):
         ms = graph_timer(step, steps, warm, steps, stream, world)
         t = ms * 1e-3 / steps
         gbs = nvfp4_bytes(m, n, k) / t / 1e9
+        floor = None
+        if m == 1:
+            def fstep(i, out=out):
+                qq, bb = qs[i % copies]
+                gq.probe_gemv_read_floor(qq, bb, out=out.reshape(-1), stream=stream)
+            tf = graph_timer(fstep, steps, warm, steps, stream, world) * 1e-3 / steps
+            floor = {"what": "the same launch with the loads only (gq_probe_gemv_read_floor)",
+                     "us": round(tf * 1e6, 3), "frac_hbm": round(nvfp4_bytes(m, n, k) / tf / 1e9 /
+                                                                   peaks["hbm_gbs"], 4),
+                     "time_over_floor": round(t / tf, 4)}
         tfl = 2 * m * n * k / t / 1e12
         key = "nvfp4_gemv_m1" if m == 1 else f"nvfp4_gemm_m{m}"
         frac_hbm = gbs / peaks["hbm_gbs"]
@@ -474,6 +501,9 @@ def nvfp4_subs(gq, dev, stream, peaks, world, steps, warm, subs):
                      "frac_bf16_tensor": round(frac_tc, 4),
                      "roofline_frac": round(max(frac_hbm, frac_tc) if m == 128 else frac_hbm, 4),
                      "l2": f"{copies} rotating weight copies"}
+        if floor is not None:
+            subs[key]["floor"] = floor
+            subs[key]["traffic"] = committed_traffic("nvfp4_gemv")
     del qs
 
 

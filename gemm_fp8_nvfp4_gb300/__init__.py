@@ -68,6 +68,7 @@ SIGNATURES = {
     "gq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint32), _I]),
     "gq_set_launch_flags": (_I, [ctypes.c_uint32]),
     "gq_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "gq_probe_gemv_read_floor": (_I, [_I, _P, _P, _P, _I64, _I64, _P]),
     "gq_get_launch_flags": (ctypes.c_uint32, []),
 }
 
@@ -445,6 +446,24 @@ def get_launch_flags() -> int:
     return int(load_library().gq_get_launch_flags())
 
 
+def probe_gemv_read_floor(w, bs=None, out=None, stream=None):
+    """The GEMV launch shape with loads only (gq_probe_gemv_read_floor): FP8
+    when bs is None (w [N, K] e4m3/uint8), else NVFP4 (w = q [N, K/2] uint8,
+    bs [N, K/16]).  Returns the checksum vector [N] bf16 (not a product)."""
+    w, wp = _u8(w, "w", 2)
+    n = w.shape[0]
+    if bs is None:
+        fmt, k, bp = 0, w.shape[1], None
+    else:
+        bs, bp = _u8(bs, "bs", 2)
+        fmt, k = 1, 2 * w.shape[1]
+    y = _out(out, (n,), torch.bfloat16, w.device)
+    _check(load_library().gq_probe_gemv_read_floor(fmt, _dev(y, "out"), wp, bp, n, k,
+                                                   _stream_handle(stream)),
+           "probe_gemv_read_floor")
+    return y
+
+
 def set_wait_limit_ns(ns: int) -> None:
     """Limit of the kernels' bounded waits on the current device (0 = the
     default 2 s); for tests of the failure path (synchronizes)."""
@@ -463,6 +482,6 @@ __all__ = [
     "nvfp4_grouped_matmul", "int8_quantize_rows", "int8_matmul",
     "fp8_materialize", "nvfp4_materialize", "device_status", "load_library", "GQError",
     "set_launch_flags", "get_launch_flags", "GQ_LAUNCH_OVERLAP_WEIGHT_READS",
-    "GQ_LAUNCH_TEST_STALL_PRODUCER", "set_wait_limit_ns",
+    "GQ_LAUNCH_TEST_STALL_PRODUCER", "set_wait_limit_ns", "probe_gemv_read_floor",
     "SIGNATURES", "LIB_PATH", "version", "status_str", "ACTIVATIONS", "Epilogue",
 ]

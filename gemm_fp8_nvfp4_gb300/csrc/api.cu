@@ -388,6 +388,18 @@ int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q, const uint8
   return gq::launch_status(gq::launch_nvfp4_materialize(c, out, kind, q, bs, N * K / 16));
 }
 
+int gq_probe_gemv_read_floor(int format, void* y, const uint8_t* w, const uint8_t* bs,
+                             int64_t N, int64_t K, cudaStream_t stream) {
+  if (format != 0 && format != 1) return GQ_ERR_DTYPE;
+  if (N < 0 || K < 0 || K % 16 != 0) return GQ_ERR_SHAPE;
+  if (N == 0 || K == 0) return GQ_OK;
+  if (!y || !w || (format == 1 && !bs)) return GQ_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(y, 2)) return GQ_ERR_ALIGN;
+  gq::Ctx c;
+  if (int s = gq::device_ctx(stream, &c)) return s;
+  return gq::launch_status(gq::launch_gemv_read_floor(c, format, y, w, bs, N, K));
+}
+
 int gq_set_wait_limit_ns(uint64_t ns) {
   gq::Ctx c;
   if (int s = gq::device_ctx(nullptr, &c)) return s;

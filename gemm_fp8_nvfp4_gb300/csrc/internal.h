@@ -66,6 +66,11 @@ cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, const Epi& ep, const void* 
                               const uint8_t* q, const uint8_t* bs, int64_t N,
                               int64_t K, float alpha);
 
+// The GEMVs' launch shapes with only the weight (and block-scale) loads:
+// format 0 = FP8 (K % 16 == 0), 1 = NVFP4.  Writes a checksum per row to y (bf16).
+cudaError_t launch_gemv_read_floor(const Ctx& c, int format, void* y, const uint8_t* w,
+                                   const uint8_t* bs, int64_t N, int64_t K);
+
 // gemm.cu
 cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
                             const uint8_t* w, int64_t M, int64_t N, int64_t K,

@@ -353,6 +353,20 @@ int gq_nvfp4_materialize(void* out, int out_dtype, const uint8_t* q,
 int gq_device_status(uint32_t* flags, int reset);
 
 /*
+ * Measurement probe (not a citation of the pages): the HBM floor of the
+ * GEMVs' launch shapes.  Runs the FP8 (format 0; w [N, K], K % 16 == 0,
+ * 16-byte aligned) or NVFP4 (format 1; w = q [N, K/2], bs [N, K/16]) GEMV
+ * kernel with its grid, CTA shape, L2 prefetch, dependent launch and weight
+ * loads unchanged but the decode and the arithmetic left out: it reads every
+ * weight and block-scale byte once and writes one checksum value per row to
+ * y ([N] bfloat16, caller-owned; an integer in [0, 128]).  The time of a call is what the GEMV of
+ * the same shape would take if its arithmetic were free.  Returns GQ_OK or a
+ * GQ_ERR code (format: GQ_ERR_DTYPE).
+ */
+int gq_probe_gemv_read_floor(int format, void* y, const uint8_t* w, const uint8_t* bs,
+                             int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * How long a bounded in-kernel wait of the current device polls before it
  * gives up (records its bit in the status word and lets the kernel unwind):
  * `ns` nanoseconds, or the default of 2 s when ns == 0.  Applies to kernels

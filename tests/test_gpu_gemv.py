@@ -312,3 +312,26 @@ def test_overlap_flag_orders_few_row_gemm(overlap_flag):
     ref = oracle.nvfp4_matmul(bits(a0), q.numpy(), bs.numpy(), s2)
     assert_within(to_f64(ct), ref, oracle.tolerance(bits(a0), oracle.decode_nvfp4(q.numpy(), bs.numpy()), s2),
                   "after torch write")
+
+
+def test_read_floor_probe():
+    """gq_probe_gemv_read_floor runs both GEMV launch shapes with loads only:
+    it returns GQ_OK, writes one checksum value per row (the number of the
+    CTA's 128 threads whose folded words have the row's bit set: an integer in
+    [0, 128]), and refuses bad arguments like the GEMVs."""
+    lib()
+    codes, _ = synth.fp8_weight(1000, 4096, seed=3)
+    y = gq.probe_gemv_read_floor(codes.to(DEV))
+    q, bs, _ = synth.nvfp4_weight(1000, 4096, seed=4)
+    y4 = gq.probe_gemv_read_floor(q.to(DEV), bs.to(DEV))
+    torch.cuda.synchronize()
+    for v in (y, y4):
+        vals = v.float().cpu()
+        assert torch.all((vals >= 0) & (vals <= 128) & (vals == vals.round()))
+    l = gq.load_library()
+    s = torch.cuda.current_stream().cuda_stream
+    w = codes.to(DEV)
+    assert l.gq_probe_gemv_read_floor(2, y.data_ptr(), w.data_ptr(), None, 1000, 4096, s) == 4
+    assert l.gq_probe_gemv_read_floor(0, y.data_ptr(), w.data_ptr(), None, 1000, 4100, s) == 2
+    assert l.gq_probe_gemv_read_floor(1, y.data_ptr(), w.data_ptr(), None, 1000, 4096, s) == 1
+    assert gq.device_status() == 0
