@@ -1236,6 +1236,7 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
     const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
     return launch<Fmt::kFp8, false, true>(c, ta, tw, nullptr, p, std::min(tiles, c.num_sms), &tx);
   }
+  if (fewrow_ok(0, M, K, a, w, nullptr)) return launch_fp8_gemm_fewrow(c, out, ep, a, w, M, N, K, alpha);
   if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, ep, a, w, M, N, K, alpha);
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
@@ -1254,6 +1255,8 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void
                               const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N, int64_t K,
                               float alpha) {
   if (K == 0) return fill_zero(c, out, ep, M * N, N, alpha);
+  if (fewrow_ok(1, M, K, a, q, bs))
+    return launch_nvfp4_gemm_fewrow(c, out, ep, a, q, bs, M, N, K, alpha);
   if (M <= skinny_max_rows() && nvfp4_skinny_ok(bs, K))
     return launch_nvfp4_gemm_skinny(c, out, ep, a, q, bs, M, N, K, alpha);
   CUtensorMap ta, tw;

@@ -103,6 +103,18 @@ cudaError_t launch_nvfp4_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                       int64_t E, int64_t max_rows,
                                       int64_t total_M, int64_t N, int64_t K);
 
+// fewrow.cu (1 <= M <= 16): register-fed mma.sync products.  fewrow_ok says
+// whether the kernel takes the call (format 0 = FP8: K % 64 == 0; 1 = NVFP4:
+// K % 128 == 0; a and w 16-byte aligned, NVFP4 bs 2-byte aligned).
+bool fewrow_ok(int format, int64_t M, int64_t K, const void* a, const uint8_t* w,
+               const uint8_t* bs);
+cudaError_t launch_fp8_gemm_fewrow(const Ctx& c, void* out, const Epi& ep, const void* a,
+                                   const uint8_t* w, int64_t M, int64_t N, int64_t K,
+                                   float alpha);
+cudaError_t launch_nvfp4_gemm_fewrow(const Ctx& c, void* out, const Epi& ep, const void* a,
+                                     const uint8_t* q, const uint8_t* bs, int64_t M, int64_t N,
+                                     int64_t K, float alpha);
+
 // gemm_skinny.cu (M <= skinny_max_rows())
 int skinny_max_rows();
 bool nvfp4_skinny_ok(const uint8_t* bs, int64_t K);   // the NVFP4 few-row kernel takes this K
