@@ -16,8 +16,8 @@
 //   * one CTA per SM, 16 warps, takes an even contiguous share of the N
 //     weight rows and walks it in groups of 32 rows (two 16-row MMA tiles;
 //     rows past the share are zero and never loaded); its warps take the K
-//     steps w, w + 16, ..., each warp issuing all loads of a step (weights
-//     and activations) before its decode and MMAs;
+//     steps w, w + 16, ..., issuing the weight loads of two steps before
+//     the decode and MMAs of the first;
 //   * in a K step, lane (g, t) (g = lane / 4, t = lane % 4) loads the 16-byte
 //     chunk t of rows g and g + 8 of each tile (FP8: 16 elements, NVFP4: 32
 //     elements = two blocks and their two scale bytes) and decodes it exactly
@@ -52,6 +52,7 @@ constexpr int kTiles = 2;                 // 16-row MMA tiles per row group
 constexpr int kGroupRows = 16 * kTiles;   // weight rows per row group
 constexpr int kMaxM = 16;                 // activation rows (two 8-column MMA tiles)
 constexpr int kFewFp8 = 0, kFewNvfp4 = 1;
+constexpr int kBatch = 2;                // K steps whose weight loads are issued together
 
 // D (16 x 8, f32) += A (16 x 16, bf16, row-major fragment) x B (16 x 8, bf16).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -148,40 +149,51 @@ k_fewrow(void* __restrict__ out, Epi ep, const uint16_t* __restrict__ a,
 #pragma unroll
         for (int e = 0; e < 4; ++e) d[i][c][e] = 0.f;
 
-    for (int64_t s = warp; s < nsteps; s += kWarps) {
-      // Every load of the step first: the weight chunks (and NVFP4 block
-      // scales) of both tiles, then the activation fragments of the step
-      // (k0 .. k0 + chunk of each token), so that one memory round trip
-      // serves the whole step.
-      const int64_t k0 = s * kStepK + t * kChunk;
-      uint4 wv[kTiles][2];
-      uint32_t sv[kTiles][2];
+    for (int64_t s0 = warp; s0 < nsteps; s0 += static_cast<int64_t>(kWarps) * kBatch) {
+      // The weight chunks (and NVFP4 block scales) of kBatch steps first, so
+      // one memory round trip serves them; then per step the activation
+      // fragments (k0 .. k0 + chunk of each token: L1 / L2 hits), the decode
+      // and the MMAs.
+      uint4 wv[kBatch][kTiles][2];
+      uint32_t sv[kBatch][kTiles][2];
 #pragma unroll
-      for (int i = 0; i < kTiles; ++i)
+      for (int b = 0; b < kBatch; ++b) {
+        const int64_t s = s0 + static_cast<int64_t>(kWarps) * b;
+        const int64_t k0 = s * kStepK + t * kChunk;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          load_chunk<F>(w, bs, ok[i][h], rows[i][h], rbytes, K, k0, wv[i][h], sv[i][h]);
-      uint4 x0[kJ / 2], x1[kJ / 2];
+        for (int i = 0; i < kTiles; ++i)
 #pragma unroll
-      for (int jj = 0; jj < kJ / 2; ++jj) {
-        x0[jj] = act8(a0, tok0, k0 + 8 * jj);
-        x1[jj] = kTwo ? act8(a1, tok1, k0 + 8 * jj) : make_uint4(0u, 0u, 0u, 0u);
+          for (int h = 0; h < 2; ++h)
+            load_chunk<F>(w, bs, ok[i][h] && s < nsteps, rows[i][h], rbytes, K, k0, wv[b][i][h],
+                          sv[b][i][h]);
       }
 #pragma unroll
-      for (int i = 0; i < kTiles; ++i) {
-        uint32_t lo[kWords], hi[kWords];
-        decode_chunk<F>(wv[i][0], sv[i][0], lo);
-        decode_chunk<F>(wv[i][1], sv[i][1], hi);
+      for (int b = 0; b < kBatch; ++b) {
+        const int64_t s = s0 + static_cast<int64_t>(kWarps) * b;
+        if (s >= nsteps) break;
+        const int64_t k0 = s * kStepK + t * kChunk;
+        uint4 x0[kJ / 2], x1[kJ / 2];
 #pragma unroll
-        for (int j = 0; j < kJ; ++j) {
-          // activations k0 + 4j .. k0 + 4j + 3: word pair (2 (j % 2), + 1) of x[j / 2]
-          const uint4& xa = x0[j >> 1];
-          mma_bf16_16816(d[i][0], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
-                         (j & 1) ? xa.z : xa.x, (j & 1) ? xa.w : xa.y);
-          if constexpr (kTwo) {
-            const uint4& xb = x1[j >> 1];
-            mma_bf16_16816(d[i][1], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
-                           (j & 1) ? xb.z : xb.x, (j & 1) ? xb.w : xb.y);
+        for (int jj = 0; jj < kJ / 2; ++jj) {
+          x0[jj] = act8(a0, tok0, k0 + 8 * jj);
+          x1[jj] = kTwo ? act8(a1, tok1, k0 + 8 * jj) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kTiles; ++i) {
+          uint32_t lo[kWords], hi[kWords];
+          decode_chunk<F>(wv[b][i][0], sv[b][i][0], lo);
+          decode_chunk<F>(wv[b][i][1], sv[b][i][1], hi);
+#pragma unroll
+          for (int j = 0; j < kJ; ++j) {
+            // activations k0 + 4j .. k0 + 4j + 3: word pair (2 (j % 2), + 1) of x[j / 2]
+            const uint4& xa = x0[j >> 1];
+            mma_bf16_16816(d[i][0], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
+                           (j & 1) ? xa.z : xa.x, (j & 1) ? xa.w : xa.y);
+            if constexpr (kTwo) {
+              const uint4& xb = x1[j >> 1];
+              mma_bf16_16816(d[i][1], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
+                             (j & 1) ? xb.z : xb.x, (j & 1) ? xb.w : xb.y);
+            }
           }
         }
       }
