@@ -98,6 +98,7 @@ constexpr uint32_t kPartStride = BN * 4 + 16;   // split-K partial row: 256 fp32
 // W8A8: K steps one CTA may sum (255 x 64 = 16320 K; every digit-plane partial
 // sum stays below 1024 x 16320 < 2^24, exact in float32).
 constexpr int kInt8MaxStepsPerCta = 255;
+constexpr int kMaxClusterSplit = 8;   // K split over at most a portable cluster
 static_assert(static_cast<int64_t>(kInt8MaxStepsPerCta) * BK * 8 == kInt8MaxK,
               "the C ABI's W8A8 K limit is eight CTAs' worth");
 constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
@@ -1074,8 +1075,16 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const uint32_t local = smem_base + r * kPartStride + c * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         int iacc[4] = {0, 0, 0, 0};   // W8A8: exact int32 sums of the ranks' partials
-        for (int q = 0; q < p.ksplit; ++q) {
-          const float4 v = tc::ld_cluster_f4(tc::map_to_rank(local, q));
+        // every rank's partial requested before the first add (the loads are
+        // in flight together), then summed in rank order
+        float4 part[kMaxClusterSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterSplit; ++q)
+          if (q < p.ksplit) part[q] = tc::ld_cluster_f4(tc::map_to_rank(local, q));
+#pragma unroll
+        for (int q = 0; q < kMaxClusterSplit; ++q) {
+          if (q >= p.ksplit) break;
+          const float4 v = part[q];
           if constexpr (F == Fmt::kInt8) {
             iacc[0] += __float_as_int(v.x); iacc[1] += __float_as_int(v.y);
             iacc[2] += __float_as_int(v.z); iacc[3] += __float_as_int(v.w);

@@ -420,12 +420,17 @@ k_wq_gemm_skinny(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       if (S == 1) {
         acc = tc::lds_f4(addr);
       } else {
-        acc = tc::ld_cluster_f4(tc::map_to_rank(addr, 0));
+        // every rank's partial requested before the first add (the loads are
+        // in flight together), then summed in rank order
+        float4 v[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          if (q < S) v[q] = tc::ld_cluster_f4(tc::map_to_rank(addr, q));
+        acc = v[0];
 #pragma unroll
         for (int q = 1; q < kMaxSplit; ++q) {
           if (q < S) {
-            const float4 v = tc::ld_cluster_f4(tc::map_to_rank(addr, q));
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
           }
         }
       }
