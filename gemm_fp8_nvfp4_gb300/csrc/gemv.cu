@@ -187,8 +187,9 @@ __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, in
 // with the decode and arithmetic left out -- each thread folds the words it
 // loaded into a checksum bit per row -- so its time is the HBM floor of this
 // launch shape (gq_probe_gemv_read_floor).
-template <int VEC, int R, int U, int T = kThreads, bool kOverlap = false, bool kFloor = false>
-__global__ void __launch_bounds__(T, 7)   // 7 CTAs per SM (<= 73 registers)
+template <int VEC, int R, int U, int T = kThreads, bool kOverlap = false, bool kFloor = false,
+          int kMinBlocks = 7>
+__global__ void __launch_bounds__(T, kMinBlocks)   // 4 rows: 7 CTAs per SM (<= 73 registers)
 k_fp8_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
            const uint8_t* __restrict__ w, int64_t N, int64_t K, float alpha) {
   constexpr int kThreads = T;
@@ -473,30 +474,48 @@ k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
 
 constexpr int kRows = 4;
 
-template <int VEC, int U>
-cudaError_t fp8_launch(const Ctx& c, int64_t grid, void* y, const Epi& ep, const void* x,
+template <int VEC, int R, int U, int MINB = 7>
+cudaError_t fp8_launch(const Ctx& c, void* y, const Epi& ep, const void* x,
                        const uint8_t* w, int64_t N, int64_t K, float alpha) {
+  const int64_t grid = (N + R - 1) / R;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {
-    return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, U, kThreads, true>,
+    return launch_kernel(c, true, k_fp8_gemv<VEC, R, U, kThreads, true, false, MINB>,
                          dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep,
                          static_cast<const uint16_t*>(x), w, N, K, alpha);
   }
-  return launch_kernel(c, true, k_fp8_gemv<VEC, kRows, U>, dim3(static_cast<unsigned>(grid)),
-                       dim3(kThreads), 0, y, ep, static_cast<const uint16_t*>(x), w, N, K, alpha);
+  return launch_kernel(c, true, k_fp8_gemv<VEC, R, U, kThreads, false, false, MINB>,
+                       dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep,
+                       static_cast<const uint16_t*>(x), w, N, K, alpha);
+}
+
+// Launch shape of the 16-byte-vector FP8 GEMV (also used by its read-floor
+// probe): a thread with exactly two vectors per row (K = 4096) issues both
+// rows' pairs in one batch (U = 2: one memory round trip instead of two;
+// 14336 x 4096 10.0 us instead of 11.1 us), else batches of four and single
+// vectors.  When such a launch's 4-row CTAs would all be resident at once
+// (N <= 4 rows x 7 CTAs x SMs), 8-row CTAs (at most 4 per SM) leave free
+// slots in which the next kernel of the stream starts its prologue and L2
+// prefetch while this one drains: 4096 x 4096 alone takes 4.1 us instead
+// of 3.5 us, but the three decode shapes in sequence take 25.5 us instead
+// of 25.9 us.
+enum class Fp8Shape { kR4U4, kR4U2, kR8U2 };
+Fp8Shape fp8_shape(const Ctx& c, int64_t N, int64_t K) {
+  if ((K / 16 + kThreads - 1) / kThreads != 2) return Fp8Shape::kR4U4;
+  return N <= 4LL * 7 * c.num_sms ? Fp8Shape::kR8U2 : Fp8Shape::kR4U2;
 }
 
 template <int VEC>
 cudaError_t fp8_dispatch(const Ctx& c, void* y, const Epi& ep, const void* x,
                          const uint8_t* w, int64_t N, int64_t K, float alpha) {
-  const int64_t grid = (N + kRows - 1) / kRows;
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  // 16-byte vectors: a thread with exactly two vectors per row (K = 4096)
-  // issues both rows' pairs in one batch (U = 2: one memory round trip
-  // instead of two; 14336 x 4096 10.0 us instead of 11.1 us); otherwise
-  // batches of four and single vectors for the rest.
-  if (VEC == 16 && (K / 16 + kThreads - 1) / kThreads == 2)
-    return fp8_launch<VEC, 2>(c, grid, y, ep, x, w, N, K, alpha);
-  return fp8_launch<VEC, (VEC == 16 ? 4 : 2)>(c, grid, y, ep, x, w, N, K, alpha);
+  if constexpr (VEC == 16) {
+    switch (fp8_shape(c, N, K)) {
+      case Fp8Shape::kR8U2: return fp8_launch<16, 8, 2, 4>(c, y, ep, x, w, N, K, alpha);
+      case Fp8Shape::kR4U2: return fp8_launch<16, kRows, 2>(c, y, ep, x, w, N, K, alpha);
+      default: return fp8_launch<16, kRows, 4>(c, y, ep, x, w, N, K, alpha);
+    }
+  }
+  return fp8_launch<VEC, kRows, 2>(c, y, ep, x, w, N, K, alpha);
 }
 
 }  // namespace
@@ -509,11 +528,19 @@ cudaError_t launch_gemv_read_floor(const Ctx& c, int format, void* y, const uint
   ep.out_kind = kOutBf16;
   const dim3 g(static_cast<unsigned>(grid));
   if (format == 0) {
-    if ((K / 16 + kThreads - 1) / kThreads == 2)
-      return launch_kernel(c, true, k_fp8_gemv<16, kRows, 2, kThreads, false, true>, g, dim3(kThreads),
-                           0, y, ep, static_cast<const uint16_t*>(nullptr), w, N, K, 1.0f);
-    return launch_kernel(c, true, k_fp8_gemv<16, kRows, 4, kThreads, false, true>, g, dim3(kThreads), 0,
-                         y, ep, static_cast<const uint16_t*>(nullptr), w, N, K, 1.0f);
+    const auto* none = static_cast<const uint16_t*>(nullptr);
+    switch (fp8_shape(c, N, K)) {
+      case Fp8Shape::kR8U2:
+        return launch_kernel(c, true, k_fp8_gemv<16, 8, 2, kThreads, false, true, 4>,
+                             dim3(static_cast<unsigned>((N + 7) / 8)), dim3(kThreads), 0, y, ep, none,
+                             w, N, K, 1.0f);
+      case Fp8Shape::kR4U2:
+        return launch_kernel(c, true, k_fp8_gemv<16, kRows, 2, kThreads, false, true>, g,
+                             dim3(kThreads), 0, y, ep, none, w, N, K, 1.0f);
+      default:
+        return launch_kernel(c, true, k_fp8_gemv<16, kRows, 4, kThreads, false, true>, g,
+                             dim3(kThreads), 0, y, ep, none, w, N, K, 1.0f);
+    }
   }
   return launch_kernel(c, true, k_nvfp4_gemv<8, kRows, 2, kThreads, false, true>, g, dim3(kThreads), 0,
                        y, ep, static_cast<const uint16_t*>(nullptr), w, bs, N, K, 1.0f);
