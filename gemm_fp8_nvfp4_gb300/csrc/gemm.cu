@@ -37,6 +37,15 @@
 //                 written by TMA (TMEM is free again before the stores land),
 //                 otherwise directly with bounds guards.
 //   warps 2, 3    idle.
+// Pair tiles (the plain FP8 / NVFP4 GEMM with M > 128): a cluster of two CTAs
+// on two SMs shares a tile of 512 A rows x 256 weight rows.  Each CTA loads
+// 256 A rows and 128 weight rows and decodes only those; the even CTA's MMA
+// thread issues tcgen05.mma.cta_group::2 (M = 256: 128 rows from each CTA's
+// A, N = 256: 128 weight rows from each CTA) and each CTA's TMEM receives the
+// sums of its own rows.  The weight bytes a CTA moves through shared memory
+// per K step halve for the same MMA work; the odd CTA's dequant and epilogue
+// warps signal the even CTA's barriers remotely, and the MMA's commits reach
+// both CTAs' barriers (multicast).
 // W8A8 (Fmt::kInt8): the A tile is int8 too and holds 128 rows.  The page's
 // int32 accumulation is kept exact on binary16 MMAs by splitting every A code
 // into two base-16 digits, a = 16 h + l (h in [-8, 8], l in [-8, 7]): the
@@ -126,6 +135,9 @@ template <> struct RawLayout<Fmt::kInt8> {
 template <Fmt F> struct Smem {
   static constexpr int kRawSt = kRawStages;     // A + raw weight ring
   static constexpr int kDeqSt = kDeqStages;     // decoded weight ring
+  static constexpr int kWRows = BN;             // weight rows this CTA loads and decodes
+  static constexpr uint32_t kWBytes = RawLayout<F>::kWBytes;
+  static constexpr uint32_t kScaleBytes = RawLayout<F>::kScaleBytes;
   static constexpr uint32_t kAStride = kABytes;
   static constexpr uint32_t kARawBytes = kABytes;   // A bytes the TMA brings per stage
   static constexpr bool kADeq = false;              // A read by the MMA from the A ring
@@ -162,6 +174,9 @@ static_assert(kAnyInTile * kAnyRowA <= 32 * BK * 2, "in-place A rows fit their 4
 struct SmemAnyK {
   static constexpr int kRawSt = 2;
   static constexpr int kDeqSt = 2;
+  static constexpr int kWRows = BN;
+  static constexpr uint32_t kWBytes = RawLayout<Fmt::kFp8>::kWBytes;   // (unused: own boxes)
+  static constexpr uint32_t kScaleBytes = 0;
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kDeqOff = kABytes;
   static constexpr uint32_t kSideOff = kABytes + kDeqBytes;
@@ -185,8 +200,45 @@ struct SmemAnyK {
   static constexpr uint32_t kWBoxBytes = 16 * kAnyWBox;
 };
 
-template <Fmt F, bool kAnyK>
-using SmemFor = typename std::conditional<kAnyK, SmemAnyK, Smem<F>>::type;
+// Pair tiles (cta_group::2): the two CTAs of a cluster pair share a tile of
+// kPairBM A rows x BN weight rows.  Each CTA holds 256 A rows (the 128-row
+// halves h = 0, 1 are tile rows 256 h + 128 rank + [0, 128)) and loads and
+// decodes 128 of the weight rows (tile rows 128 rank + [0, 128)); one thread
+// of the even CTA issues M = 256, N = 256 MMAs that read both CTAs' operands,
+// and each CTA's TMEM receives the sums of its own A rows.  Per K step a CTA
+// moves half the weight bytes through shared memory that a one-CTA tile of
+// 256 rows does, for the same MMA work.
+constexpr int kPairBM = 512;
+constexpr int kPairWRows = BN / 2;
+template <Fmt F> struct SmemPair {
+  static constexpr int kRawSt = 4;
+  static constexpr int kDeqSt = 2;
+  static constexpr int kWRows = kPairWRows;
+  static constexpr uint32_t kWBytes = RawLayout<F>::kWBytes / 2;
+  static constexpr uint32_t kScaleBytes = RawLayout<F>::kScaleBytes / 2;
+  static constexpr uint32_t kAStride = kABytes;
+  static constexpr uint32_t kARawBytes = kABytes;
+  static constexpr bool kADeq = false;
+  static constexpr uint32_t kDeqAOff = 0;
+  static constexpr uint32_t kDeqStride = kDeqBytes / 2;     // 128 decoded rows
+  static constexpr uint32_t kDeqOff = 0;
+  static constexpr uint32_t kAOff = kDeqOff + kDeqSt * kDeqStride;
+  static constexpr uint32_t kWOff = kAOff + kRawSt * kABytes;
+  static constexpr uint32_t kSOff = kWOff + kRawSt * kWBytes;
+  static constexpr uint32_t kBarOff = (kSOff + kRawSt * kScaleBytes + 7) & ~7u;
+  static constexpr uint32_t kNumBars = 2 * kRawSt + 2 * kDeqSt + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kStageOff = (kMiscOff + 16 + 1023) & ~1023u;
+  static constexpr uint32_t kStageBytes = 4 * 2 * 2048;
+  static constexpr uint32_t kTotal = kStageOff + kStageBytes;
+  static constexpr uint32_t kAlloc = kTotal + 1024;
+};
+static_assert(SmemPair<Fmt::kFp8>::kAlloc <= 232448 && SmemPair<Fmt::kNvfp4>::kAlloc <= 232448,
+              "pair stages and output staging fit in shared memory");
+
+template <Fmt F, bool kAnyK, bool kPair>
+using SmemFor = typename std::conditional<
+    kAnyK, SmemAnyK, typename std::conditional<kPair, SmemPair<F>, Smem<F>>::type>::type;
 
 // W8A8: raw int8 A (8 KB, 128 rows) and W (16 KB) stages, 64-byte swizzle,
 // and decoded stages holding the weight and the two digit planes of A as
@@ -194,6 +246,9 @@ using SmemFor = typename std::conditional<kAnyK, SmemAnyK, Smem<F>>::type;
 template <> struct Smem<Fmt::kInt8> {
   static constexpr int kRawSt = kRawStages;
   static constexpr int kDeqSt = kDeqStages;
+  static constexpr int kWRows = BN;
+  static constexpr uint32_t kWBytes = RawLayout<Fmt::kInt8>::kWBytes;
+  static constexpr uint32_t kScaleBytes = 0;
   static constexpr uint32_t kARawBytes = UMMA_M * BK;         // 8 KB: 128 rows of int8 A
   static constexpr uint32_t kAStride = kARawBytes;
   static constexpr bool kADeq = true;                         // MMA reads A from the decoded stage
@@ -230,7 +285,7 @@ struct Problem {
   uint32_t* status;
   float alpha;
   int M, N, K;                 // M = total rows for grouped
-  int bm;                      // A rows per tile of the plain GEMM (BM; W8A8: UMMA_M)
+  int bm;                      // A rows per tile (BM; W8A8: UMMA_M; pair tiles: kPairBM)
   int num_n_tiles;
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
@@ -288,7 +343,7 @@ __device__ __forceinline__ int grouped_num_tiles(const Problem& p) {
   for (int z = 0; z < p.G; ++z) {
     int s;
     const int rows = group_rows(p, z, &s);
-    total += ((rows + BM - 1) / BM) * p.num_n_tiles;
+    total += ((rows + p.bm - 1) / p.bm) * p.num_n_tiles;
   }
   return total;
 }
@@ -299,11 +354,11 @@ __device__ __forceinline__ Tile grouped_tile(const Problem& p, int t) {
   for (int z = 0; z < p.G; ++z) {
     int s;
     const int rows = group_rows(p, z, &s);
-    const int mt = (rows + BM - 1) / BM;
+    const int mt = (rows + p.bm - 1) / p.bm;
     const int cnt = mt * p.num_n_tiles;
     if (t < cnt) {
-      tl.m0 = s + (t % mt) * BM;
-      tl.m_end = min(tl.m0 + BM, s + rows);
+      tl.m0 = s + (t % mt) * p.bm;
+      tl.m_end = min(tl.m0 + p.bm, s + rows);
       tl.n0 = (t / mt) * BN;
       const int id = __ldg(p.expert_ids + z);
       tl.expert = (id >= 0 && id < p.E) ? id : -1;
@@ -387,21 +442,22 @@ __device__ __forceinline__ int digit_sum(uint32_t hi_bits, uint32_t lo_bits) {
 
 // ----------------------------------------------------------------- kernel --
 
-template <Fmt F, bool kGrouped, bool kAnyK>
+template <Fmt F, bool kGrouped, bool kAnyK, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
           const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_o,
           const uint8_t* __restrict__ scales_g, Problem p) {
-  using L = SmemFor<F, kAnyK>;
+  static_assert(!kPair || (F != Fmt::kInt8 && !kAnyK), "pair tiles: FP8 / NVFP4 with K % 16 == 0");
+  using L = SmemFor<F, kAnyK, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* full_raw = bars;
-  uint64_t* empty_raw = bars + kRawStages;
-  uint64_t* full_deq = bars + 2 * kRawStages;
-  uint64_t* empty_deq = full_deq + kDeqStages;
-  uint64_t* tmem_full = empty_deq + kDeqStages;
+  uint64_t* empty_raw = bars + L::kRawSt;
+  uint64_t* full_deq = bars + 2 * L::kRawSt;
+  uint64_t* empty_deq = full_deq + L::kDeqSt;
+  uint64_t* tmem_full = empty_deq + L::kDeqSt;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* drain = tmem_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -410,6 +466,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t smem_base = tc::smem_u32(smem);
+  // Pair tiles: rank 0 of the pair issues the MMAs; the other roles run in
+  // both CTAs on the CTA's own rows.
+  const int prank = kPair ? static_cast<int>(tc::cluster_ctarank()) : 0;
 
   if (threadIdx.x == 0) {
     // The raw stage is full after the copies (+ the NVFP4 scale copies).  It
@@ -417,25 +476,33 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // any K: the loader warps finish with a stage before the MMA starts).
     constexpr uint32_t kRawArrivals = (kAnyK || F == Fmt::kNvfp4) ? 1 + 32 : 1;
     constexpr uint32_t kRawReleases = kAnyK ? 1 : 1 + kDeqWarps;
-    for (int s = 0; s < kRawStages; ++s) {
+    // Pair tiles: the even CTA's full_deq and tmem_empty also count the odd
+    // CTA's dequant and epilogue warps (remote arrivals); the MMA's commits
+    // reach the barriers of both CTAs.
+    for (int s = 0; s < L::kRawSt; ++s) {
       tc::mbar_init(&full_raw[s], kRawArrivals);
       tc::mbar_init(&empty_raw[s], kRawReleases);
     }
-    for (int s = 0; s < kDeqStages; ++s) {
-      tc::mbar_init(&full_deq[s], kDeqWarps);
+    for (int s = 0; s < L::kDeqSt; ++s) {
+      tc::mbar_init(&full_deq[s], kPair ? 2 * kDeqWarps : kDeqWarps);
       tc::mbar_init(&empty_deq[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&tmem_full[s], 1);
-      tc::mbar_init(&tmem_empty[s], 4);
+      tc::mbar_init(&tmem_empty[s], kPair ? 8 : 4);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == kWarpMma) {
-    tc::tmem_alloc(tmem_slot, kTmemCols);
-    tc::tmem_relinquish();
+    if constexpr (kPair) {
+      tc::tmem_alloc_pair(tmem_slot, kTmemCols);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(tmem_slot, kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   if (!kAnyK && warp == kWarpTma && lane == 0 && p.num_k_blocks > 0 && (!kGrouped || p.E > 0)) {
     tc::tma_prefetch_desc(&tmap_a);
@@ -450,17 +517,28 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     if (p.w_groups > 0) tc::tma_prefetch_desc(&tmap_w);
   }
   tc::tc_fence_before();
-  __syncthreads();
+  // Pair tiles: the peer's barriers are initialized before any remote arrival
+  // or multicast commit can reach them.
+  if constexpr (kPair) tc::cluster_sync();
+  else __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int total_tiles = num_tiles<kGrouped>(p);
   // Split-K (small M): the CTAs of a cluster share one tile, rank r owns the
   // K steps [kb0, kb1); otherwise a CTA walks tiles persistently over all K.
+  // Pair tiles: the pair (cluster) walks the tiles persistently.
   const bool split = p.ksplit > 1;
   const int crank = split ? static_cast<int>(blockIdx.x) % p.ksplit : 0;
-  const int t_first = split ? static_cast<int>(blockIdx.x) / p.ksplit : static_cast<int>(blockIdx.x);
-  const int t_step = split ? total_tiles : static_cast<int>(gridDim.x);
+  const int unit = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  const int t_first = split ? static_cast<int>(blockIdx.x) / p.ksplit : unit;
+  const int t_step = split ? total_tiles : units;
+  // Pair tiles: this CTA's first weight row within the tile's BN rows, and
+  // the offset of its A rows within each 256-row half of the tile.
+  const int w_row0 = kPair ? prank * kPairWRows : 0;
+  const int a_row0 = kPair ? prank * UMMA_M : 0;
+  constexpr int kHalfRows = kPair ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
   const int kb0 = split ? crank * p.kb_per_split : 0;
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
@@ -480,8 +558,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     auto prefetch_w = [&](const Tile& pt, int pkb) {
       if (lane != 0 || !pt.valid || pt.expert < 0) return;
       constexpr int kBpk = (F == Fmt::kNvfp4) ? BK / 2 : BK;   // weight bytes per row per K step
-      if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * kBpk, pt.n0, pt.expert);
-      else tc::tma_prefetch_l2_2d(&tmap_w, pkb * kBpk, pt.n0);
+      if constexpr (kGrouped) tc::tma_prefetch_l2_3d(&tmap_w, pkb * kBpk, pt.n0 + w_row0, pt.expert);
+      else tc::tma_prefetch_l2_2d(&tmap_w, pkb * kBpk, pt.n0 + w_row0);
     };
     if (t_first < total_tiles) {
       const Tile first = get_tile<kGrouped>(p, t_first);
@@ -494,39 +572,50 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       Tile next{};
       next.valid = false;
       if (tn < total_tiles) next = get_tile<kGrouped>(p, tn);
+      // Pair tiles: the second 128-row half of this CTA's A rows only when
+      // the tile has more than 256 rows.
+      const int a_halves = (kPair && tl.m_end - tl.m0 <= kHalfRows) ? 1 : 2;
       for (int kb = kb0; kb < nkb; ++kb) {
         if (kb + kL2Prefetch < nkb) prefetch_w(tl, kb + kL2Prefetch);
         else if (kb + kL2Prefetch - nkb < nkb && !split) prefetch_w(next, kb + kL2Prefetch - nkb);
-        if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
+        if (!tc::mbar_wait<kPair>(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
         }
         uint8_t* a_dst = smem + L::kAOff + s * L::kAStride;
-        uint8_t* w_dst = smem + L::kWOff + s * RawLayout<F>::kWBytes;
+        uint8_t* w_dst = smem + L::kWOff + s * L::kWBytes;
         if (lane == 0) {
-          tc::mbar_arrive_expect_tx(&full_raw[s], L::kARawBytes + RawLayout<F>::kWBytes);
-          tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0);
+          if constexpr (kPair) {
+            tc::mbar_arrive_expect_tx(&full_raw[s], a_halves * kAHalfBytes + L::kWBytes);
+            for (int h = 0; h < a_halves; ++h)
+              tc::tma_load_2d(a_dst + h * kAHalfBytes, &tmap_a, &full_raw[s], kb * BK,
+                              tl.m0 + h * kHalfRows + a_row0);
+          } else {
+            tc::mbar_arrive_expect_tx(&full_raw[s], L::kARawBytes + L::kWBytes);
+            tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0);
+          }
           constexpr int kBpk = (F == Fmt::kNvfp4) ? BK / 2 : BK;
-          if constexpr (kGrouped) tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0, tl.expert);
-          else tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0);
+          if constexpr (kGrouped)
+            tc::tma_load_3d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0 + w_row0, tl.expert);
+          else tc::tma_load_2d(w_dst, &tmap_w, &full_raw[s], kb * kBpk, tl.n0 + w_row0);
         }
         if constexpr (F == Fmt::kNvfp4) {
           // Block scales: 4 bytes (4 blocks of 16) per weight row per stage;
           // grouped: rows of expert e start at e * N.
-          uint8_t* s_dst = smem + L::kSOff + s * RawLayout<F>::kScaleBytes;
+          uint8_t* s_dst = smem + L::kSOff + s * L::kScaleBytes;
           const int ks = p.K / 16;
           const int64_t row_base = kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0;
 #pragma unroll
-          for (int i = 0; i < BN / 32; ++i) {
+          for (int i = 0; i < L::kWRows / 32; ++i) {
             const int r = lane + 32 * i;
-            const int n = tl.n0 + r;
+            const int n = tl.n0 + w_row0 + r;
             const bool in = n < p.N;
             const uint8_t* src = scales_g + ((row_base + (in ? n : 0)) * ks + kb * 4);
             tc::cp_async_4(s_dst + r * 4, src, in ? 4u : 0u);
           }
           tc::cp_async_mbar_arrive_noinc(&full_raw[s]);
         }
-        if (++s == kRawStages) { s = 0; ph ^= 1; }
+        if (++s == L::kRawSt) { s = 0; ph ^= 1; }
       }
     }
     // Drain: make sure no copy issued by this warp is still landing in shared
@@ -534,8 +623,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     if (lane == 0) {
       int ds = s;
       uint32_t dph = ph;
-      for (int i = 0; i < kRawStages; ++i) {
-        if (--ds < 0) { ds = kRawStages - 1; dph ^= 1; }
+      for (int i = 0; i < L::kRawSt; ++i) {
+        if (--ds < 0) { ds = L::kRawSt - 1; dph ^= 1; }
         tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
       }
     }
@@ -644,10 +733,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma && prank == 0) {
     // ------------------------------------------------------- MMA issuer --
-    constexpr uint32_t kIdesc =
-        F == Fmt::kInt8 ? tc::idesc_f16_f32(UMMA_M, BN) : tc::idesc_bf16_f32(UMMA_M, BN);
+    // Pair tiles: M = 256 MMAs over both CTAs' operands, from rank 0 only.
+    constexpr uint32_t kIdesc = F == Fmt::kInt8 ? tc::idesc_f16_f32(UMMA_M, BN)
+                                                : tc::idesc_bf16_f32(kPair ? 2 * UMMA_M : UMMA_M, BN);
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     int it = 0;
@@ -659,13 +749,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       ++it;
       // (Any K: the rows are in residue order, spread over both halves.)
       // (W8A8: the halves are the two digit planes of the tile's 128 rows.)
-      const bool two_halves = F == Fmt::kInt8 || (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > UMMA_M;
+      const bool two_halves = F == Fmt::kInt8 || (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > kHalfRows;
       // Both accumulators free (the epilogue of the previous tile has read them).
-      if (!tc::mbar_wait(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
+      if (!tc::mbar_wait<kPair>(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
       tc::tc_fence_after();
       for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma) ||
-            !tc::mbar_wait(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
+            !tc::mbar_wait<kPair>(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
@@ -680,25 +770,40 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             const uint64_t a0 = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
             const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
             const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-            tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
-            // A tile with at most 128 rows (ragged end of M or of a group)
-            // needs only the first half; the second accumulator is unused.
-            if (two_halves) tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
+            // A tile with at most 128 rows (pair tiles: 256; the ragged end
+            // of M or of a group) needs only the first half; the second
+            // accumulator is unused.
+            if constexpr (kPair) {
+              tc::mma_bf16_pair(tmem_base, a0, bd, kIdesc, accum);
+              if (two_halves) tc::mma_bf16_pair(tmem_base + BN, a1, bd, kIdesc, accum);
+            } else {
+              tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
+              if (two_halves) tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
+            }
           }
-          tc::mma_commit(&empty_raw[s]);
-          tc::mma_commit(&empty_deq[d]);
+          if constexpr (kPair) {
+            tc::mma_commit_pair(&empty_raw[s], 3);
+            tc::mma_commit_pair(&empty_deq[d], 3);
+          } else {
+            tc::mma_commit(&empty_raw[s]);
+            tc::mma_commit(&empty_deq[d]);
+          }
         }
         __syncwarp();
         if (++s == L::kRawSt) { s = 0; ph ^= 1; }
         if (++d == L::kDeqSt) { d = 0; dph ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) tc::mma_commit(&tmem_full[0]);
+      if (lane == 0) {
+        if constexpr (kPair) tc::mma_commit_pair(&tmem_full[0], 3);
+        else tc::mma_commit(&tmem_full[0]);
+      }
       __syncwarp();
     }
     // Drain: every MMA issued by this thread completes before TMEM is freed.
     if (lane == 0) {
-      tc::mma_commit(drain);
+      if constexpr (kPair) tc::mma_commit_pair(drain, 1);
+      else tc::mma_commit(drain);
       tc::mbar_wait_quiet(drain, 0, 100000000ull);
     }
     __syncwarp();
@@ -799,7 +904,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
   } else if (!kAnyK && warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ---------------------------------------------------------- dequant --
-    const int row = threadIdx.x - kDeqWarp0 * 32;  // 0..255: weight row in the tile
+    // One thread per weight row of the CTA's tile; pair tiles (128 rows per
+    // CTA): two threads per row, each decoding half of the row's K step.
+    const int tid = threadIdx.x - kDeqWarp0 * 32;   // 0..255
+    const int row = tid % L::kWRows;                // weight row in the CTA's part of the tile
+    const int part = tid / L::kWRows;               // pair tiles: which half of the K step
+    constexpr int kParts = kDeqWarps * 32 / L::kWRows;
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     bool ok = true;
@@ -808,11 +918,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       if (!tl.valid || tl.expert < 0) continue;
       for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant) ||
-            !tc::mbar_wait(&empty_deq[d], dph ^ 1, abort_flag, p.status, kStatusTimeoutDequant)) {
+            !tc::mbar_wait<kPair>(&empty_deq[d], dph ^ 1, abort_flag, p.status, kStatusTimeoutDequant)) {
           ok = false;
           break;
         }
-        const uint32_t w_addr = smem_base + L::kWOff + s * RawLayout<F>::kWBytes;
+        const uint32_t w_addr = smem_base + L::kWOff + s * L::kWBytes;
         const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
         if constexpr (F == Fmt::kInt8) {
           // Rows of 64 int8 codes (TMA 64-byte swizzle: chunk c at
@@ -838,7 +948,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         } else if constexpr (F == Fmt::kFp8) {
           // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 4 / kParts; ++i) {
+            const int c = part * (4 / kParts) + i;
             const uint4 v = tc::lds128(w_addr + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
             uint4 lo, hi;
             fp8x16_to_bf16(v, lo, hi);
@@ -847,9 +958,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           }
         } else {
           // Row of 32 packed bytes, TMA 32-byte swizzle: chunk c at c ^ ((row >> 2) & 1).
-          const uint32_t sc = tc::lds32(smem_base + L::kSOff + s * RawLayout<F>::kScaleBytes + row * 4);
+          const uint32_t sc = tc::lds32(smem_base + L::kSOff + s * L::kScaleBytes + row * 4);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int i = 0; i < 2 / kParts; ++i) {
+            const int c = part * (2 / kParts) + i;
             const uint4 v = tc::lds128(w_addr + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
             const uint16_t s0 = e4m3_to_f16(sc >> (16 * c));
             const uint16_t s1 = e4m3_to_f16(sc >> (16 * c + 8));
@@ -865,11 +977,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         tc::fence_proxy_async_smem();   // make the generic stores visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          tc::mbar_arrive(&full_deq[d]);
+          // Pair tiles: the MMA issuer (rank 0) waits for both CTAs' rows.
+          if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&full_deq[d]), 0));
+          else tc::mbar_arrive(&full_deq[d]);
           tc::mbar_arrive(&empty_raw[s]);
         }
-        if (++s == kRawStages) { s = 0; ph ^= 1; }
-        if (++d == kDeqStages) { d = 0; dph ^= 1; }
+        if (++s == L::kRawSt) { s = 0; ph ^= 1; }
+        if (++d == L::kDeqSt) { d = 0; dph ^= 1; }
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -889,7 +1003,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const int per16 = 16 / es;                        // elements per 16-byte store
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-          const int m = tl.m0 + h * UMMA_M + g * 32 + lane;
+          const int m = tl.m0 + h * kHalfRows + a_row0 + g * 32 + lane;
           if (m >= tl.m_end) continue;
           const int cend = min(BN, p.N - tl.n0);
           const int64_t o = static_cast<int64_t>(m) * p.N + tl.n0;
@@ -904,7 +1018,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       }
       const uint32_t acc_ph = it & 1;
       ++it;
-      if (!tc::mbar_wait(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
+      if (!tc::mbar_wait<kPair>(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
       tc::tc_fence_after();
       if (split) {
         // This CTA's raw fp32 partial of rows [0, 128) -> shared memory (the
@@ -944,12 +1058,14 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
       const bool residue_rows = kAnyK && !p.a_tma;
       // W8A8: one half of output rows (the TMEM halves are its digit planes).
-      const int halves = F == Fmt::kInt8 ? 1 : (residue_rows || tl.m_end - tl.m0 > UMMA_M) ? 2 : 1;
+      const int halves = F == Fmt::kInt8 ? 1 : (residue_rows || tl.m_end - tl.m0 > kHalfRows) ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
-        // TMEM lane h * 128 + 32 g + lane holds tile row h * 128 + 32 g + lane,
-        // or (any K, residue order) tile row 8 lane + 4 h + g.
-        const int m = residue_rows ? tl.m0 + 8 * lane + 4 * h + g : tl.m0 + h * UMMA_M + g * 32 + lane;
+        // Lane 32 g + lane of TMEM half h holds tile row h * 128 + 32 g + lane
+        // (pair tiles: h * 256 + 128 rank + 32 g + lane), or (any K, residue
+        // order) tile row 8 lane + 4 h + g.
+        const int m = residue_rows ? tl.m0 + 8 * lane + 4 * h + g
+                                   : tl.m0 + h * kHalfRows + a_row0 + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
 #pragma unroll 1
@@ -978,7 +1094,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           // TMA store of the warp's 32 x 32 box (16-bit outputs, all rows of
           // the box inside the tile or, for the plain GEMM, past the end of
           // the output where the store clips them): every lane stages its row.
-          const int mbox = tl.m0 + h * UMMA_M + g * 32;
+          const int mbox = tl.m0 + h * kHalfRows + a_row0 + g * 32;
           const bool use_box = L::kStageBytes > 0 && !kAnyK && p.tma_out && n < p.N &&
                                mbox < tl.m_end && (!kGrouped || mbox + 32 <= tl.m_end);
           if (use_box) {
@@ -1049,7 +1165,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
+      if (lane == 0) {
+        if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&tmem_empty[0]), 0));
+        else tc::mbar_arrive(&tmem_empty[0]);
+      }
     }
     // Every TMA store of this warp has completed before the CTA exits.
     if (lane == 0) tc::bulk_wait_all();
@@ -1110,9 +1229,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
     tc::cluster_sync();   // no CTA leaves while a peer still reads its partial
   }
+  // Pair tiles: neither CTA frees its TMEM or leaves while rank 0's MMAs may
+  // still read the peer's shared memory or a remote arrival is on its way.
+  if constexpr (kPair) tc::cluster_sync();
   if (warp == kWarpMma) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair) tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tc::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -1126,12 +1249,12 @@ __global__ void k_fill_scaled_zero(void* out, Epi ep, int64_t count, int64_t N, 
 
 // --------------------------------------------------------------- host --
 
-template <Fmt F, bool kGrouped, bool kAnyK = false>
+template <Fmt F, bool kGrouped, bool kAnyK = false, bool kPair = false>
 cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, const uint8_t* scales,
                    const Problem& p, int grid, const CUtensorMap* tx = nullptr,
                    const CUtensorMap* to = nullptr) {
-  auto kern = k_wq_gemm<F, kGrouped, kAnyK>;
-  const uint32_t smem = SmemFor<F, kAnyK>::kAlloc;
+  auto kern = k_wq_gemm<F, kGrouped, kAnyK, kPair>;
+  const uint32_t smem = SmemFor<F, kAnyK, kPair>::kAlloc;
   Problem pl = p;
   pl.stall_producer = (!kAnyK && c.test_stall_producer) ? 1 : 0;
   // The shared-memory opt-in is set once per device (it is not a stream
@@ -1150,14 +1273,44 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.ksplit > 1 ? p.ksplit : 1;
+  attr[0].val.clusterDim.x = kPair ? 2 : p.ksplit > 1 ? p.ksplit : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.ksplit > 1 ? 1 : 0;
+  cfg.numAttrs = (kPair || p.ksplit > 1) ? 1 : 0;
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
   return cudaLaunchKernelEx(&cfg, kern, ta, tw, tx ? *tx : unused, to ? *to : unused, scales, pl);
+}
+
+// CTA pairs (clusters of 2 one-CTA-per-SM blocks) the GPU holds at once,
+// queried once per device (pair kernels of both formats have one CTA per SM).
+int max_pairs(const Ctx& c) {
+  static std::atomic<int> cached[64];
+  const int dev = c.device & 63;
+  int v = cached[dev].load(std::memory_order_acquire);
+  if (v > 0) return v;
+  auto kern = k_wq_gemm<Fmt::kFp8, false, false, true>;
+  const uint32_t smem = SmemPair<Fmt::kFp8>::kAlloc;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (c.num_sms / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  v = n > 0 ? std::min(n, c.num_sms / 2) : std::max(1, c.num_sms / 2);
+  cached[dev].store(v, std::memory_order_release);
+  return v;
 }
 
 cudaError_t fill_zero(const Ctx& c, void* out, const Epi& ep, int64_t count, int64_t N, float alpha) {
@@ -1247,17 +1400,20 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
   }
   if (fewrow_ok(0, M, K, a, w, nullptr)) return launch_fp8_gemm_fewrow(c, out, ep, a, w, M, N, K, alpha);
   if (M <= skinny_max_rows()) return launch_fp8_gemm_skinny(c, out, ep, a, w, M, N, K, alpha);
+  // Pair tiles: A in 128-row boxes, each CTA's 128 weight rows in one box.
   CUtensorMap ta, tw;
-  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, UMMA_M,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))
+      !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kPairWRows,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   Problem p = base_problem(c, out, ep, M, N, K, alpha);
-  const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
-  const int grid = plan_split(c, p, tiles);
+  p.bm = kPairBM;
+  const int tiles = ((p.M + kPairBM - 1) / kPairBM) * p.num_n_tiles;
+  const int grid = 2 * std::min(tiles, max_pairs(c));
   CUtensorMap to;
   p.tma_out = output_map(ep, out, M, N, &to);
-  return launch<Fmt::kFp8, false>(c, ta, tw, nullptr, p, grid, nullptr, &to);
+  return launch<Fmt::kFp8, false, false, true>(c, ta, tw, nullptr, p, grid, nullptr, &to);
 }
 
 cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void* a,
@@ -1268,6 +1424,22 @@ cudaError_t launch_nvfp4_gemm(const Ctx& c, void* out, const Epi& ep, const void
     return launch_nvfp4_gemm_fewrow(c, out, ep, a, q, bs, M, N, K, alpha);
   if (M <= skinny_max_rows() && nvfp4_skinny_ok(bs, K))
     return launch_nvfp4_gemm_skinny(c, out, ep, a, q, bs, M, N, K, alpha);
+  if (M > UMMA_M) {
+    // Pair tiles, as launch_fp8_gemm.
+    CUtensorMap ta, tw;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, UMMA_M,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K / 2, N, K / 2, BK / 2, kPairWRows,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+      return cudaErrorInvalidValue;
+    Problem p = base_problem(c, out, ep, M, N, K, alpha);
+    p.bm = kPairBM;
+    const int tiles = ((p.M + kPairBM - 1) / kPairBM) * p.num_n_tiles;
+    const int grid = 2 * std::min(tiles, max_pairs(c));
+    CUtensorMap to;
+    p.tma_out = output_map(ep, out, M, N, &to);
+    return launch<Fmt::kNvfp4, false, false, true>(c, ta, tw, bs, p, grid, nullptr, &to);
+  }
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1317,7 +1489,10 @@ cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_
 
 // The grouped problem shared by both formats, and its persistent grid: an
 // upper bound of the work list (the exact count needs the device offsets),
-// capped at one CTA per SM.
+// capped at one CTA per SM.  (Pair tiles of 512 rows were measured slower
+// here: experts of 500-570 rows leave 30-60-row tails that cost a 256-row
+// pair MMA half each, 1.34x padded MMA rows against 1.14x with 256-row
+// one-CTA tiles.)
 static Problem grouped_problem(const Ctx& c, void* out, const Epi& ep, const uint32_t* a_offsets,
                                const int32_t* expert_ids, const float* expert_scales, int64_t G,
                                int64_t E, int64_t max_rows, int64_t total_M, int64_t N, int64_t K,

@@ -44,6 +44,26 @@ def test_fp8_gemm_shapes(m, n, k):
     check_fp8(m, n, k, seed=m + n + k)
 
 
+# M > 128 runs on CTA pairs: tiles of 512 rows (each CTA of the pair holds
+# rows 256 h + 128 rank + [0, 128) of the tile) and 256 weight rows (128 per
+# CTA).  Row counts around 256 and 512, and N with the odd CTA's weight rows
+# partly or wholly past the end.
+PAIR_EDGES = [(129, 256, 64), (256, 200, 64), (257, 129, 128), (511, 300, 192), (512, 128, 64),
+              (513, 384, 64), (1000, 520, 256), (1537, 260, 128)]
+
+
+@pytest.mark.parametrize("m,n,k", PAIR_EDGES)
+def test_fp8_gemm_pair_tile_edges(m, n, k):
+    lib()
+    check_fp8(m, n, k, seed=m + 2 * n + k)
+
+
+@pytest.mark.parametrize("m,n,k", PAIR_EDGES)
+def test_nvfp4_gemm_pair_tile_edges(m, n, k):
+    lib()
+    check_nvfp4(m, n, k, seed=m + 3 * n + k)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_fp8_gemm_bf16_and_f32_out(out_dtype):
     lib()

@@ -59,6 +59,19 @@ def test_grouped_small_edge_cases():
     run_grouped(a, stack, scales, offs, ids, max_rows=200)
 
 
+def test_grouped_pair_tile_rows():
+    """Groups of 255 to 1100 rows: one or both 256-row halves of a 512-row
+    pair tile, and groups over several pair tiles with ragged tails; N with
+    the odd CTA's weight rows partly past the end."""
+    lib()
+    stack, scales = synth.fp8_expert_stack(3, 300, 128, seed=11)
+    sizes = [255, 256, 257, 511, 512, 513, 1100, 0, 1, 700]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    ids = [0, 1, 2, 0, 1, -1, 2, 1, 0, 1]
+    a = synth.bf16_activations(offs[-1], 128, seed=12)
+    run_grouped(a, stack, scales, offs, ids, max_rows=max(sizes))
+
+
 def test_grouped_raw_no_scales_bf16():
     lib()
     stack, _ = synth.fp8_expert_stack(2, 256, 256, seed=3)

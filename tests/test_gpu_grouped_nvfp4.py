@@ -68,6 +68,17 @@ def test_nvfp4_grouped_small_edge_cases():
     run_grouped(a, q, bs, s2, offs, ids, max_rows=200)
 
 
+def test_nvfp4_grouped_pair_tile_rows():
+    """As the FP8 test: groups of 255 to 1100 rows over 512-row pair tiles."""
+    lib()
+    q, bs, s2 = synth.nvfp4_expert_stack(3, 300, 128, seed=11)
+    sizes = [255, 256, 257, 511, 512, 513, 1100, 0, 1, 700]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    ids = [0, 1, 2, 0, 1, -1, 2, 1, 0, 1]
+    a = synth.bf16_activations(offs[-1], 128, seed=12)
+    run_grouped(a, q, bs, s2, offs, ids, max_rows=max(sizes))
+
+
 @pytest.mark.parametrize("k", [64, 192, 1024])
 def test_nvfp4_grouped_k_multiples_of_64(k):
     """K a multiple of 64 but not of the 128-element k-step where it is odd."""
