@@ -368,7 +368,7 @@ __device__ __forceinline__ void load_xf(const uint16_t* __restrict__ x, int64_t 
 
 // kFloor: weight and scale loads only (as in k_fp8_gemv).
 template <int VB, int R, int U, int T = kThreads, bool kOverlap = false, bool kFloor = false>
-__global__ void __launch_bounds__(T, 6)   // 6 CTAs per SM (<= 85 registers)
+__global__ void __launch_bounds__(T, 7)   // 7 CTAs per SM (<= 73 registers)
 k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
              const uint8_t* __restrict__ q, const uint8_t* __restrict__ bs, int64_t N,
              int64_t K, float alpha) {
@@ -566,7 +566,10 @@ cudaError_t launch_nvfp4_gemv(const Ctx& c, void* y, const Epi& ep, const void* 
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   // 4 rows per CTA, two 8-byte vectors (one 16-element block each) per row
   // per step: measured best at N = K = 4096 against 16-byte vectors and
-  // other row / vector / CTA-size splits.
+  // other row / vector / CTA-size splits.  At most 7 CTAs per SM (72
+  // registers) put the 1024 CTAs of N = 4096 in one wave (1064 slots); with 6
+  // per SM, 112 CTAs ran as a second wave (3.91 us against 3.56 us; 8 per SM
+  // 4.12 us, 8-row CTAs 3.89 us).
   const int64_t grid = (N + kRows - 1) / kRows;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {
