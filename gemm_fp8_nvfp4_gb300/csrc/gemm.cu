@@ -233,7 +233,33 @@ template <Fmt F> struct SmemPair {
   static constexpr uint32_t kTotal = kStageOff + kStageBytes;
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
-static_assert(SmemPair<Fmt::kFp8>::kAlloc <= 232448 && SmemPair<Fmt::kNvfp4>::kAlloc <= 232448,
+// W8A8 pair tiles: 256 output rows (128 per CTA) x 256 weight rows; the
+// decoded stage holds the CTA's 128 weight rows and the two digit planes of
+// its 128 A rows as binary16 (W at +0, high digits at +16 KB, low at +32 KB).
+template <> struct SmemPair<Fmt::kInt8> {
+  static constexpr int kRawSt = 4;
+  static constexpr int kDeqSt = 2;
+  static constexpr int kWRows = kPairWRows;
+  static constexpr uint32_t kWBytes = RawLayout<Fmt::kInt8>::kWBytes / 2;   // 8 KB
+  static constexpr uint32_t kScaleBytes = 0;
+  static constexpr uint32_t kARawBytes = UMMA_M * BK;                       // 8 KB
+  static constexpr uint32_t kAStride = kARawBytes;
+  static constexpr bool kADeq = true;
+  static constexpr uint32_t kDeqAOff = kDeqBytes / 2;                       // 16 KB
+  static constexpr uint32_t kDeqStride = kDeqBytes / 2 + kABytes;           // 48 KB
+  static constexpr uint32_t kDeqOff = 0;
+  static constexpr uint32_t kAOff = kDeqOff + kDeqSt * kDeqStride;
+  static constexpr uint32_t kWOff = kAOff + kRawSt * kAStride;
+  static constexpr uint32_t kSOff = kWOff + kRawSt * kWBytes;
+  static constexpr uint32_t kBarOff = kSOff;
+  static constexpr uint32_t kNumBars = 2 * kRawSt + 2 * kDeqSt + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kStageOff = 0, kStageBytes = 0;   // no TMA-store staging
+  static constexpr uint32_t kTotal = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kTotal + 1024;
+};
+static_assert(SmemPair<Fmt::kFp8>::kAlloc <= 232448 && SmemPair<Fmt::kNvfp4>::kAlloc <= 232448 &&
+                  SmemPair<Fmt::kInt8>::kAlloc <= 232448,
               "pair stages and output staging fit in shared memory");
 
 template <Fmt F, bool kAnyK, bool kPair>
@@ -447,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
           const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_o,
           const uint8_t* __restrict__ scales_g, Problem p) {
-  static_assert(!kPair || (F != Fmt::kInt8 && !kAnyK), "pair tiles: FP8 / NVFP4 with K % 16 == 0");
+  static_assert(!kPair || !kAnyK, "pair tiles: K % 16 == 0");
   using L = SmemFor<F, kAnyK, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -538,7 +564,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   // the offset of its A rows within each 256-row half of the tile.
   const int w_row0 = kPair ? prank * kPairWRows : 0;
   const int a_row0 = kPair ? prank * UMMA_M : 0;
-  constexpr int kHalfRows = kPair ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
+  // (W8A8: the two MMA halves are the digit planes of the same rows.)
+  constexpr int kHalfRows = (kPair && F != Fmt::kInt8) ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
   const int kb0 = split ? crank * p.kb_per_split : 0;
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
@@ -585,7 +612,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         uint8_t* a_dst = smem + L::kAOff + s * L::kAStride;
         uint8_t* w_dst = smem + L::kWOff + s * L::kWBytes;
         if (lane == 0) {
-          if constexpr (kPair) {
+          if constexpr (kPair && F == Fmt::kInt8) {
+            tc::mbar_arrive_expect_tx(&full_raw[s], L::kARawBytes + L::kWBytes);
+            tc::tma_load_2d(a_dst, &tmap_a, &full_raw[s], kb * BK, tl.m0 + a_row0);
+          } else if constexpr (kPair) {
             tc::mbar_arrive_expect_tx(&full_raw[s], a_halves * kAHalfBytes + L::kWBytes);
             for (int h = 0; h < a_halves; ++h)
               tc::tma_load_2d(a_dst + h * kAHalfBytes, &tmap_a, &full_raw[s], kb * BK,
@@ -736,8 +766,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   } else if (warp == kWarpMma && prank == 0) {
     // ------------------------------------------------------- MMA issuer --
     // Pair tiles: M = 256 MMAs over both CTAs' operands, from rank 0 only.
-    constexpr uint32_t kIdesc = F == Fmt::kInt8 ? tc::idesc_f16_f32(UMMA_M, BN)
-                                                : tc::idesc_bf16_f32(kPair ? 2 * UMMA_M : UMMA_M, BN);
+    constexpr int kMmaM = kPair ? 2 * UMMA_M : UMMA_M;
+    constexpr uint32_t kIdesc =
+        F == Fmt::kInt8 ? tc::idesc_f16_f32(kMmaM, BN) : tc::idesc_bf16_f32(kMmaM, BN);
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
     int it = 0;
@@ -926,24 +957,29 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
         if constexpr (F == Fmt::kInt8) {
           // Rows of 64 int8 codes (TMA 64-byte swizzle: chunk c at
-          // c ^ ((row >> 1) & 3)) -> binary16, exactly: weight row `row`, and
-          // decoded A row `row` = digit row >> 7 (0: high, 1: low) of A row
-          // row & 127.
+          // c ^ ((row >> 1) & 3)) -> binary16, exactly: weight row `row`
+          // (pair tiles: half of its chunks), and decoded A row `tid` =
+          // digit tid >> 7 (0: high, 1: low) of A row tid & 127.
           const uint32_t a_raw = smem_base + L::kAOff + s * L::kAStride;
           const uint32_t a_dq = b_addr + L::kDeqAOff;
-          const int ar = row & (UMMA_M - 1);
-          const int digit = row >> 7;
+          const int ar = tid & (UMMA_M - 1);
+          const int digit = tid >> 7;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 4 / kParts; ++i) {
+            const int c = part * (4 / kParts) + i;
             const uint32_t src = row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
             uint4 lo, hi;
             s8x16_to_f16(tc::lds128(w_addr + src), lo, hi);
             tc::sts128(b_addr + sw128_off(row, 2 * c), lo);
             tc::sts128(b_addr + sw128_off(row, 2 * c + 1), hi);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 lo, hi;
             const uint32_t asrc = ar * 64 + ((c ^ ((ar >> 1) & 3)) << 4);
             s8x16_digit_to_f16(tc::lds128(a_raw + asrc), digit, lo, hi);
-            tc::sts128(a_dq + sw128_off(row, 2 * c), lo);
-            tc::sts128(a_dq + sw128_off(row, 2 * c + 1), hi);
+            tc::sts128(a_dq + sw128_off(tid, 2 * c), lo);
+            tc::sts128(a_dq + sw128_off(tid, 2 * c + 1), hi);
           }
         } else if constexpr (F == Fmt::kFp8) {
           // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
@@ -1460,6 +1496,20 @@ cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_
   // K = 0: every sum is 0, so the output is the epilogue of 0.
   if (K == 0) return fill_zero(c, out, ep, M * N, N, 0.f);
   if (K > kInt8MaxK) return cudaErrorInvalidValue;   // refused earlier by the C ABI
+  if (M > UMMA_M && (K + BK - 1) / BK <= kInt8MaxStepsPerCta) {
+    // Pair tiles: 256 output rows (128 A rows per CTA) x 256 weight rows.
+    CUtensorMap ta, tw;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, UMMA_M, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, BK, kPairWRows,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    Problem p = base_problem(c, out, ep, M, N, K, 1.0f);
+    p.bm = 2 * UMMA_M;
+    p.a_scale = a_scale;
+    p.b_scale = b_scale;
+    const int tiles = ((p.M + p.bm - 1) / p.bm) * p.num_n_tiles;
+    return launch<Fmt::kInt8, false, false, true>(c, ta, tw, nullptr, p, 2 * std::min(tiles, max_pairs(c)));
+  }
   CUtensorMap ta, tw;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, UMMA_M, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B))

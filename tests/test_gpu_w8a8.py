@@ -103,6 +103,17 @@ def test_int8_matmul_exact(m, n, k):
     run_matmul(qa, sa, qb, sb)
 
 
+@pytest.mark.parametrize("m,n,k", [(129, 129, 64), (256, 200, 128), (257, 300, 256), (700, 520, 192)])
+def test_int8_matmul_pair_tile_edges(m, n, k):
+    """M > 128 runs on CTA pairs: tiles of 256 rows (128 per CTA) and 256
+    weight rows (128 per CTA); row counts around the tile edges, N with the
+    odd CTA's weight rows partly or wholly past the end."""
+    lib()
+    qa, sa = synth.int8_codes(m, k, seed=2 * m + k)
+    qb, sb = synth.int8_weight(n, k, seed=3 * n + k)
+    run_matmul(qa, sa, qb, sb)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
 def test_int8_matmul_out_types(out_dtype):
     lib()
