@@ -238,7 +238,7 @@ template <Fmt F> struct SmemPair {
 // its 128 A rows as binary16 (W at +0, high digits at +16 KB, low at +32 KB).
 template <> struct SmemPair<Fmt::kInt8> {
   static constexpr int kRawSt = 4;
-  static constexpr int kDeqSt = 2;
+  static constexpr int kDeqSt = 3;   // 350 us with 2 decoded stages, 337 us with 3
   static constexpr int kWRows = kPairWRows;
   static constexpr uint32_t kWBytes = RawLayout<Fmt::kInt8>::kWBytes / 2;   // 8 KB
   static constexpr uint32_t kScaleBytes = 0;
