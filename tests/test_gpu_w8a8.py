@@ -51,11 +51,46 @@ def check_quantize(m, k, seed, special=False):
 @pytest.mark.parametrize("m,k", [(1, 16), (3, 64), (257, 4096), (64, 8192), (5, 8208),
                                  (7, 100), (33, 5), (2, 1), (2048, 4096)])
 def test_quantize_rows_exact(m, k):
-    """Codes and scales bit for bit; 2048 x 4096 (8 M elements) puts about a
-    thousand quotients within 2^-14 of a half-integer, where the kernel
-    replaces its reciprocal product by the division."""
+    """Codes and scales bit for bit (rows with exact ties to even, zero
+    rows, K with and without the register kernel)."""
     lib()
     check_quantize(m, k, seed=m + k, special=True)
+
+
+def quantize_domain_rows():
+    """One row per positive bf16 absmax a whose scale a / 127 is a normal
+    float32: a itself, then every bf16 magnitude in [a / 256, a] (1025
+    patterns, or down to zero) with both signs, zero-padded to K = 2064.
+    Every quotient x / scale with |code| >= 1 that the quantizer can meet
+    is in there."""
+    top = np.arange(0x0080, 0x7F80, dtype=np.int32)            # positive normal bf16
+    a = (top.astype(np.uint32) << 16).view(np.float32)
+    top = top[(a / np.float32(127.0)) >= np.float32(2.0 ** -126)]
+    k = 2064
+    rows = np.zeros((top.size, k), dtype=np.uint16)
+    mags = np.maximum(top[:, None] - np.arange(0, 1025, dtype=np.int32)[None, :], 0)
+    rows[:, 0] = top
+    rows[:, 1:1026] = mags
+    rows[:, 1026:2051] = mags | 0x8000
+    return torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16)
+
+
+def test_quantize_exhaustive_quotients():
+    """The register kernel divides by the row's scale with Markstein's
+    correction step (one reciprocal per row, a product, a fused residual and
+    a fused correction): its codes must equal the IEEE float32 division's on
+    every quotient it can meet.  Codes and scales bit for bit against the
+    oracle for every normal scale and every bf16 activation from absmax / 256
+    to absmax, both signs (31 K rows, 65 M quotients)."""
+    lib()
+    x = quantize_domain_rows()
+    q, s = gq.int8_quantize_rows(x.to(DEV))
+    torch.cuda.synchronize()
+    want_q, want_s = oracle.int8_quantize_rows(bits(x))
+    got_q = q.cpu().numpy()
+    bad = np.argwhere(got_q != want_q)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at row, col {bad[:3].tolist()}"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32)), "scales differ"
 
 
 def test_quantize_rows_unaligned_rows():
