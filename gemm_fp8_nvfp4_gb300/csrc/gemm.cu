@@ -262,9 +262,44 @@ static_assert(SmemPair<Fmt::kFp8>::kAlloc <= 232448 && SmemPair<Fmt::kNvfp4>::kA
                   SmemPair<Fmt::kInt8>::kAlloc <= 232448,
               "pair stages and output staging fit in shared memory");
 
+// Any-K pair tiles: each CTA realigns its 256 rows of A (tile rows
+// 256 rank + [0, 256), residue order as SmemAnyK) and decodes 128 weight rows
+// (residue boxes of 8 groups of 16 rows); three stages.
+constexpr int kAnyPairWGroups = 8;
+constexpr uint32_t kAnyPairWBox = kAnyPairWGroups * kAnyRowW;   // 640: W box of one residue
+struct SmemAnyKPair {
+  static constexpr int kRawSt = 3;
+  static constexpr int kDeqSt = 3;
+  static constexpr int kWRows = kPairWRows;
+  static constexpr uint32_t kWBytes = RawLayout<Fmt::kFp8>::kWBytes;   // (unused: own boxes)
+  static constexpr uint32_t kScaleBytes = 0;
+  static constexpr uint32_t kAOff = 0;
+  static constexpr uint32_t kDeqOff = kABytes;
+  static constexpr uint32_t kSideOff = kABytes + kDeqBytes / 2;
+  static constexpr uint32_t kWOff = kSideOff + 8 * kAnySideSlot;
+  static constexpr uint32_t kPartAOff = kWOff + 16 * kAnyPairWBox;     // <= 7 rows of A
+  static constexpr uint32_t kPartWOff = kPartAOff + 1024;              // <= 15 rows of W
+  static constexpr uint32_t kStage = (kPartWOff + 1280 + 1023) & ~1023u;
+  static constexpr uint32_t kAStride = kStage;
+  static constexpr uint32_t kARawBytes = kABytes;
+  static constexpr bool kADeq = false;
+  static constexpr uint32_t kDeqAOff = 0;
+  static constexpr uint32_t kDeqStride = kStage;
+  static constexpr uint32_t kBarOff = kRawSt * kStage;
+  static constexpr uint32_t kNumBars = 2 * kRawSt + 2 * kDeqSt + 4 + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kStageOff = 0, kStageBytes = 0;   // no TMA-store staging
+  static constexpr uint32_t kTotal = kMiscOff + 16;
+  static constexpr uint32_t kAlloc = kTotal + 1024;
+  static constexpr uint32_t kABoxBytes = SmemAnyK::kABoxBytes;
+  static constexpr uint32_t kWBoxBytes = 16 * kAnyPairWBox;
+};
+static_assert(SmemAnyKPair::kAlloc <= 232448, "any-K pair stages fit in shared memory");
+
 template <Fmt F, bool kAnyK, bool kPair>
 using SmemFor = typename std::conditional<
-    kAnyK, SmemAnyK, typename std::conditional<kPair, SmemPair<F>, Smem<F>>::type>::type;
+    kAnyK, typename std::conditional<kPair, SmemAnyKPair, SmemAnyK>::type,
+    typename std::conditional<kPair, SmemPair<F>, Smem<F>>::type>::type;
 
 // W8A8: raw int8 A (8 KB, 128 rows) and W (16 KB) stages, 64-byte swizzle,
 // and decoded stages holding the weight and the two digit planes of A as
@@ -413,10 +448,10 @@ __device__ __forceinline__ int num_tiles(const Problem& p) {
 // ------------------------------------------------------ any-K loading --
 
 // Where the raw window of residue r, group index i (tile row 8 i + r) of a
-// stage lands, relative to the stage.
-__device__ __forceinline__ uint32_t any_raw_a_off(int r, int i) {
+// stage lands, relative to the stage (side_off: the layout's side area).
+__device__ __forceinline__ uint32_t any_raw_a_off(int r, int i, uint32_t side_off) {
   return i < kAnyInTile ? static_cast<uint32_t>(r * 4096 + i * kAnyRowA)
-                        : SmemAnyK::kSideOff + r * kAnySideSlot + (i - kAnyInTile) * kAnyRowA;
+                        : side_off + r * kAnySideSlot + (i - kAnyInTile) * kAnyRowA;
 }
 
 // The bytes [off, off + 4 N) of in[] (off = 0..15, a per-row constant), as
@@ -473,8 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
           const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_o,
           const uint8_t* __restrict__ scales_g, Problem p) {
-  static_assert(!kPair || !kAnyK, "pair tiles: K % 16 == 0");
+  static_assert(!kPair || !kAnyK || (F == Fmt::kFp8 && !kGrouped), "any-K pair tiles: plain FP8");
   using L = SmemFor<F, kAnyK, kPair>;
+  // The any-K roles' layout (the same type as L when kAnyK; the roles are
+  // compiled, never run, in the other instantiations).
+  using LA = typename std::conditional<kPair, SmemAnyKPair, SmemAnyK>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -563,9 +601,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   // Pair tiles: this CTA's first weight row within the tile's BN rows, and
   // the offset of its A rows within each 256-row half of the tile.
   const int w_row0 = kPair ? prank * kPairWRows : 0;
-  const int a_row0 = kPair ? prank * UMMA_M : 0;
-  // (W8A8: the two MMA halves are the digit planes of the same rows.)
-  constexpr int kHalfRows = (kPair && F != Fmt::kInt8) ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
+  const int a_row0 = kPair ? prank * (kAnyK ? BM : UMMA_M) : 0;
+  // (W8A8: the two MMA halves are the digit planes of the same rows.  Any
+  // K: CTA r holds tile rows 256 r + [0, 256) -- in residue order, or in
+  // order as halves of 128 -- and both halves are always issued.)
+  constexpr int kHalfRows = (kPair && F != Fmt::kInt8 && !kAnyK) ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
   const int kb0 = split ? crank * p.kb_per_split : 0;
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
@@ -671,12 +711,21 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     const uint8_t* w_end = p.w_g + static_cast<int64_t>(p.N) * K;
     const int a_full = 8 * p.a_groups;             // rows covered by the A maps
     const int w_full = 16 * p.w_groups;            // rows covered by the W map
+    // This CTA's rows of a tile (pair tiles: 256 A rows and 128 weight rows).
+    auto cta_rows = [&](const Tile& tt, int& m0c, int& m1c, int& n0c, int& n1c) {
+      m0c = tt.m0 + a_row0;
+      m1c = min(m0c + BM, tt.m_end);
+      n0c = tt.n0 + w_row0;
+      n1c = min(n0c + LA::kWRows, p.N);
+    };
     auto prefetch_tile = [&](int pt_i) {
       if (pt_i >= total_tiles) return;
       const Tile pt = get_tile<kGrouped>(p, pt_i);
       if (!pt.valid || pt.expert < 0) return;
-      prefetch_span_l2(p.w_g, pt.n0 * K + kb0 * BK, static_cast<int64_t>(min(pt.n0 + BN, p.N)) * K, lane);
-      prefetch_span_l2(a_g, 2 * (pt.m0 * K + kb0 * BK), 2 * static_cast<int64_t>(pt.m_end) * K, lane);
+      int m0c, m1c, n0c, n1c;
+      cta_rows(pt, m0c, m1c, n0c, n1c);
+      if (n1c > n0c) prefetch_span_l2(p.w_g, n0c * K + kb0 * BK, static_cast<int64_t>(n1c) * K, lane);
+      if (m1c > m0c) prefetch_span_l2(a_g, 2 * (m0c * K + kb0 * BK), 2 * static_cast<int64_t>(m1c) * K, lane);
     };
     // One 16-byte chunk at the 16-byte-aligned address src; `any` is a valid
     // address passed when no byte is read.
@@ -685,7 +734,8 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const uint32_t n = left >= 16 ? 16u : left > 0 ? static_cast<uint32_t>(left) : 0u;
       tc::cp_async_16(dst, n ? src : any, n);
     };
-    constexpr uint32_t kTx0 = SmemAnyK::kABoxBytes, kTx1 = SmemAnyK::kWBoxBytes;
+    constexpr uint32_t kTx0 = LA::kABoxBytes, kTx1 = LA::kWBoxBytes;
+    constexpr uint32_t kWBoxStride = kPair ? kAnyPairWBox : kAnyWBox;   // one residue's W box
     // K % 8 == 0: A's rows are 16-byte strided and come as one plain tiled
     // box per stage (128-byte swizzle, the MMA's layout); only W needs the
     // residue boxes.
@@ -698,35 +748,37 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const Tile tl = get_tile<kGrouped>(p, t);
       prefetch_tile(t + t_step);
       if (!tl.valid || tl.expert < 0) continue;
-      const bool a_part = !p.a_tma && tl.m_end > a_full;
-      const bool w_part = min(tl.n0 + BN, p.N) > w_full;
+      int m0c, m1c, n0c, n1c;
+      cta_rows(tl, m0c, m1c, n0c, n1c);
+      const bool a_part = !p.a_tma && m1c > a_full;
+      const bool w_part = n1c > w_full;
       for (int kb = kb0; kb < nkb; ++kb) {
-        if (!tc::mbar_wait(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
+        if (!tc::mbar_wait<kPair>(&empty_raw[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) {
           ok = false;
           break;
         }
         const int64_t k0 = static_cast<int64_t>(kb) * BK;
-        uint8_t* st = smem + s * SmemAnyK::kStage;
+        uint8_t* st = smem + s * LA::kStage;
         if (lane == 0) {
           tc::mbar_arrive_expect_tx(&full_raw[s], tx);
           if (p.a_tma) {
-            tc::tma_load_2d(st, &tmap_a, &full_raw[s], static_cast<int>(k0), tl.m0);
+            tc::tma_load_2d(st, &tmap_a, &full_raw[s], static_cast<int>(k0), m0c);
           } else if (p.a_groups > 0) {
-            const int g0 = tl.m0 / 8;
+            const int g0 = m0c / 8;
 #pragma unroll 1
             for (int r = 0; r < 8; ++r) {
               const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(7));
-              tc::tma_load_2d(st + any_raw_a_off(r, 0), &tmap_a, &full_raw[s], x0, g0);
-              tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile), &tmap_x, &full_raw[s], x0,
+              tc::tma_load_2d(st + any_raw_a_off(r, 0, LA::kSideOff), &tmap_a, &full_raw[s], x0, g0);
+              tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile, LA::kSideOff), &tmap_x, &full_raw[s], x0,
                               g0 + kAnyInTile);
             }
           }
           if (p.w_groups > 0) {
-            const int g0 = tl.n0 / 16;
+            const int g0 = n0c / 16;
 #pragma unroll 1
             for (int r = 0; r < 16; ++r) {
               const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(15));
-              tc::tma_load_2d(st + SmemAnyK::kWOff + r * kAnyWBox, &tmap_w, &full_raw[s], x0, g0);
+              tc::tma_load_2d(st + LA::kWOff + r * kWBoxStride, &tmap_w, &full_raw[s], x0, g0);
             }
           }
         }
@@ -734,9 +786,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           for (int c = lane; c < 7 * 9; c += 32) {
             const int r = c / 9, j = c - 9 * r;
             const int m = a_full + r;
-            if (m < tl.m0 || m >= tl.m_end) continue;
+            if (m < m0c || m >= m1c) continue;
             const uintptr_t w0 = reinterpret_cast<uintptr_t>(a_g + 2 * (m * K + k0)) & ~static_cast<uintptr_t>(15);
-            copy_chunk(st + SmemAnyK::kPartAOff + r * kAnyRowA + 16 * j,
+            copy_chunk(st + LA::kPartAOff + r * kAnyRowA + 16 * j,
                        reinterpret_cast<const uint8_t*>(w0) + 16 * j, a_end, a_g);
           }
         }
@@ -744,22 +796,22 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           for (int c = lane; c < 15 * 5; c += 32) {
             const int r = c / 5, j = c - 5 * r;
             const int n = w_full + r;
-            if (n < tl.n0 || n >= p.N || n >= tl.n0 + BN) continue;
+            if (n < n0c || n >= n1c) continue;
             const uintptr_t w0 = reinterpret_cast<uintptr_t>(p.w_g + n * K + k0) & ~static_cast<uintptr_t>(15);
-            copy_chunk(st + SmemAnyK::kPartWOff + r * kAnyRowW + 16 * j,
+            copy_chunk(st + LA::kPartWOff + r * kAnyRowW + 16 * j,
                        reinterpret_cast<const uint8_t*>(w0) + 16 * j, w_end, p.w_g);
           }
         }
         tc::cp_async_mbar_arrive_noinc(&full_raw[s]);
-        if (++s == SmemAnyK::kRawSt) { s = 0; ph ^= 1; }
+        if (++s == LA::kRawSt) { s = 0; ph ^= 1; }
       }
     }
     // Drain: no copy may still land when the CTA exits.
     if (lane == 0) {
       int ds = s;
       uint32_t dph = ph;
-      for (int i = 0; i < SmemAnyK::kRawSt; ++i) {
-        if (--ds < 0) { ds = SmemAnyK::kRawSt - 1; dph ^= 1; }
+      for (int i = 0; i < LA::kRawSt; ++i) {
+        if (--ds < 0) { ds = LA::kRawSt - 1; dph ^= 1; }
         tc::mbar_wait_quiet(&full_raw[ds], dph, 100000000ull);
       }
     }
@@ -846,11 +898,17 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // the swizzled tile: residue u + 8 (g & 1), group index (u + g / 2) mod 16
     // for t = 8 g + u.  Each raw window is shifted by its fixed misalignment,
     // the K tail of the last stage is zeroed, and rows past the end are zero.
+    // Pair tiles (128 weight rows per CTA, group index mod 8): threads t and
+    // t + 128 share a weight row, each realigning and decoding half of it.
+    constexpr int kWParts = kDeqWarps * 32 / LA::kWRows;   // threads per weight row
+    constexpr int kWWords = 16 / kWParts;                  // code words per thread
+    constexpr uint32_t kWBoxStride = kPair ? kAnyPairWBox : kAnyWBox;
     const int t = threadIdx.x - kDeqWarp0 * 32;
     const int ar = t >> 5, ai = t & 31;               // A residue, group index
-    const int wr = (t & 7) + 8 * ((t >> 3) & 1);      // W residue
-    const int wi = ((t & 7) + (t >> 4)) & 15;         // W group index
-    const int wrow = 16 * wi + wr;                    // W tile row
+    const int u = t % LA::kWRows, wpart = t / LA::kWRows;
+    const int wr = (u & 7) + 8 * ((u >> 3) & 1);      // W residue
+    const int wi = ((u & 7) + (u >> 4)) & (LA::kWRows / 16 - 1);   // W group index
+    const int wrow = 16 * wi + wr;                    // W row in the CTA's part of the tile
     const int64_t K = p.K;
     const int a_full = 8 * p.a_groups;
     const int w_full = 16 * p.w_groups;
@@ -862,21 +920,23 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     for (int tt = t_first; tt < total_tiles && ok; tt += t_step) {
       const Tile tl = get_tile<kGrouped>(p, tt);
       if (!tl.valid || tl.expert < 0) continue;
-      const int m = tl.m0 + 8 * ai + ar;
-      const bool a_act = m < tl.m_end;
-      const uint32_t a_src = m < a_full ? any_raw_a_off(ar, ai)
-                                        : SmemAnyK::kPartAOff + (m - a_full) * kAnyRowA;
-      const int n = tl.n0 + wrow;
+      const int m0c = tl.m0 + a_row0;                 // this CTA's rows of the tile
+      const int m = m0c + 8 * ai + ar;
+      const bool a_act = m < min(m0c + BM, tl.m_end);
+      const uint32_t a_src = m < a_full ? any_raw_a_off(ar, ai, LA::kSideOff)
+                                        : LA::kPartAOff + (m - a_full) * kAnyRowA;
+      const int n = tl.n0 + w_row0 + wrow;
       const bool w_act = n < p.N;
-      const uint32_t w_src = n < w_full ? SmemAnyK::kWOff + wr * kAnyWBox + wi * kAnyRowW
-                                        : SmemAnyK::kPartWOff + (n - w_full) * kAnyRowW;
+      const uint32_t w_src = (n < w_full ? LA::kWOff + wr * kWBoxStride + wi * kAnyRowW
+                                         : LA::kPartWOff + (n - w_full) * kAnyRowW) +
+                             32 * wpart;
       for (int kb = kb0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant)) {
           ok = false;
           break;
         }
         const int kv = min(BK, p.K - kb * BK);     // valid K of this stage, >= 1
-        const uint32_t st = smem_base + s * SmemAnyK::kStage;
+        const uint32_t st = smem_base + s * LA::kStage;
         if (!p.a_tma) {
           uint32_t out[32];
           if (a_act) {
@@ -899,27 +959,30 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
                        make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]));
         }
         {
+          // This thread's kWWords code words of its row: bytes
+          // [32 wpart, 32 wpart + 4 kWWords) of the stage's 64.
           constexpr uint16_t kOne = 0x3C00;         // 1.0 in f16
-          uint32_t code[16];
+          uint32_t code[kWWords];
           if (w_act) {
-            uint32_t in[20];
+            uint32_t in[kWWords + 4];
 #pragma unroll
-            for (int c = 0; c < 5; ++c) {
+            for (int c = 0; c < kWWords / 4 + 1; ++c) {
               const uint4 v = tc::lds128(st + w_src + 16 * c);
               in[4 * c] = v.x; in[4 * c + 1] = v.y; in[4 * c + 2] = v.z; in[4 * c + 3] = v.w;
             }
-            realign_words<16>(in, off_w, code);
-            if (kv < BK) mask_tail<16>(code, kv);
+            realign_words<kWWords>(in, off_w, code);
+            if (kv < BK) mask_tail<kWWords>(code, kv - 32 * wpart);
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) code[i] = 0u;
+            for (int i = 0; i < kWWords; ++i) code[i] = 0u;
           }
-          const uint32_t dst = st + SmemAnyK::kDeqOff;
+          const uint32_t dst = st + LA::kDeqOff;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int i = 0; i < kWWords / 2; ++i) {
+            const int c = (kWWords / 2) * wpart + i;   // 16-byte chunk of the bf16 row
             uint32_t h0, h1, h2, h3;
-            e4m3x4_to_h2x2(code[2 * c], h0, h1);
-            e4m3x4_to_h2x2(code[2 * c + 1], h2, h3);
+            e4m3x4_to_h2x2(code[2 * i], h0, h1);
+            e4m3x4_to_h2x2(code[2 * i + 1], h2, h3);
             tc::sts128(dst + sw128_off(wrow, c),
                        make_uint4(f32x2_hi_to_bf16x2(h2_scale_f32(h0, kOne)),
                                   f32x2_hi_to_bf16x2(h2_scale_f32(h1, kOne)),
@@ -929,8 +992,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         tc::fence_proxy_async_smem();   // make the generic stores visible to the tensor core
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full_deq[s]);
-        if (++s == SmemAnyK::kRawSt) { s = 0; ph ^= 1; }
+        if (lane == 0) {
+          // Pair tiles: the MMA issuer (rank 0) waits for both CTAs' rows.
+          if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&full_deq[s]), 0));
+          else tc::mbar_arrive(&full_deq[s]);
+        }
+        if (++s == LA::kRawSt) { s = 0; ph ^= 1; }
       }
     }
   } else if (!kAnyK && warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
@@ -1100,7 +1167,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         // Lane 32 g + lane of TMEM half h holds tile row h * 128 + 32 g + lane
         // (pair tiles: h * 256 + 128 rank + 32 g + lane), or (any K, residue
         // order) tile row 8 lane + 4 h + g.
-        const int m = residue_rows ? tl.m0 + 8 * lane + 4 * h + g
+        const int m = residue_rows ? tl.m0 + a_row0 + 8 * lane + 4 * h + g
                                    : tl.m0 + h * kHalfRows + a_row0 + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
@@ -1427,10 +1494,19 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
          !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72,
                     32 - kAnyInTile, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
+    // M > 256: pair tiles (each CTA realigns its 256 rows of A and decodes
+    // 128 weight rows: W boxes of 8 groups).
+    const bool pair = M > BM;
     if (p.w_groups > 0 &&
-        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 16 * K, N / 16, 16 * K, kAnyRowW, 16,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 16 * K, N / 16, 16 * K, kAnyRowW,
+                   pair ? kAnyPairWGroups : 16, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
+    if (pair) {
+      p.bm = kPairBM;
+      const int tiles = ((p.M + kPairBM - 1) / kPairBM) * p.num_n_tiles;
+      return launch<Fmt::kFp8, false, true, true>(c, ta, tw, nullptr, p,
+                                                   2 * std::min(tiles, max_pairs(c)), &tx);
+    }
     const int tiles = ((p.M + BM - 1) / BM) * p.num_n_tiles;
     return launch<Fmt::kFp8, false, true>(c, ta, tw, nullptr, p, std::min(tiles, c.num_sms), &tx);
   }

@@ -57,6 +57,17 @@ def test_anyk_shapes(m, n, k):
     check(m, n, k, seed=m + n + k)
 
 
+# M > 256 runs on CTA pairs: each CTA realigns 256 rows of A (tile rows
+# 256 rank + [0, 256)) and decodes 128 weight rows.  Rows just past 256 and
+# 512, N below 16 (no weight box at all) or with the odd CTA's weight rows
+# partly or wholly past the end, K with and without the plain A box.
+@pytest.mark.parametrize("m,n,k", [(257, 129, 72), (511, 129, 100), (600, 200, 100), (777, 15, 33),
+                                   (1030, 130, 4104), (513, 260, 4100)])
+def test_anyk_pair_edges(m, n, k):
+    lib()
+    check(m, n, k, seed=2 * m + n + k)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
 def test_anyk_out_types(out_dtype):
     lib()
