@@ -3,6 +3,8 @@
 import os
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -11,9 +13,6 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
-
-
-import pytest
 
 
 @pytest.fixture(autouse=True, scope="module")
