@@ -327,7 +327,7 @@ def run_ours(args, rank, local, world):
             "unit": "GB/s",
             "frac": round(value / world / peaks["hbm_gbs"], 4),
             "peak_source": peaks["source"],
-            "kernel": "k_fp8_gemv<16,R,U,128> (R x U = 8 x 2 for 4096 x 4096, 4 x 2 for 14336 x 4096, 4 x 4 for 4096 x 14336)",
+            "kernel": "k_fp8_gemv<16,R,U,128> (R x U = 8 x 2 for K = 4096, 4 x 4 for K = 14336)",
             "traffic": committed_traffic("fp8_gemv"),
             "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         },

@@ -490,19 +490,18 @@ cudaError_t fp8_launch(const Ctx& c, void* y, const Epi& ep, const void* x,
 }
 
 // Launch shape of the 16-byte-vector FP8 GEMV (also used by its read-floor
-// probe): a thread with exactly two vectors per row (K = 4096) issues both
-// rows' pairs in one batch (U = 2: one memory round trip instead of two;
-// 14336 x 4096 10.0 us instead of 11.1 us), else batches of four and single
-// vectors.  When such a launch's 4-row CTAs would all be resident at once
-// (N <= 4 rows x 7 CTAs x SMs), 8-row CTAs (at most 4 per SM) leave free
-// slots in which the next kernel of the stream starts its prologue and L2
-// prefetch while this one drains: 4096 x 4096 alone takes 4.1 us instead
-// of 3.5 us, but the three decode shapes in sequence take 25.5 us instead
-// of 25.9 us.
-enum class Fp8Shape { kR4U4, kR4U2, kR8U2 };
-Fp8Shape fp8_shape(const Ctx& c, int64_t N, int64_t K) {
-  if ((K / 16 + kThreads - 1) / kThreads != 2) return Fp8Shape::kR4U4;
-  return N <= 4LL * 7 * c.num_sms ? Fp8Shape::kR8U2 : Fp8Shape::kR4U2;
+// probe).  A thread with exactly two vectors per row (K = 4096) issues all
+// of its rows' vectors in one batch (U = 2: one memory round trip instead of
+// two), in 8-row CTAs (at most 4 per SM) whose free slots let the next
+// kernel of the stream start its prologue and L2 prefetch while this one
+// drains; alone, 4096 x 4096 takes 4.1-4.5 us instead of 3.5 us and
+// 14336 x 4096 11.6 us instead of 11.0 us with 4-row CTAs, but the three
+// decode shapes in sequence take 26.3 us instead of 26.7 us (4-row CTAs for
+// 14336 x 4096 only; measured back to back on one GPU).  Otherwise
+// (K = 14336) 4-row CTAs take a batch of four vectors, then single ones.
+enum class Fp8Shape { kR4U4, kR8U2 };
+Fp8Shape fp8_shape(const Ctx&, int64_t, int64_t K) {
+  return (K / 16 + kThreads - 1) / kThreads == 2 ? Fp8Shape::kR8U2 : Fp8Shape::kR4U4;
 }
 
 template <int VEC>
@@ -511,7 +510,6 @@ cudaError_t fp8_dispatch(const Ctx& c, void* y, const Epi& ep, const void* x,
   if constexpr (VEC == 16) {
     switch (fp8_shape(c, N, K)) {
       case Fp8Shape::kR8U2: return fp8_launch<16, 8, 2, 4>(c, y, ep, x, w, N, K, alpha);
-      case Fp8Shape::kR4U2: return fp8_launch<16, kRows, 2>(c, y, ep, x, w, N, K, alpha);
       default: return fp8_launch<16, kRows, 4>(c, y, ep, x, w, N, K, alpha);
     }
   }
@@ -534,9 +532,6 @@ cudaError_t launch_gemv_read_floor(const Ctx& c, int format, void* y, const uint
         return launch_kernel(c, true, k_fp8_gemv<16, 8, 2, kThreads, false, true, 4>,
                              dim3(static_cast<unsigned>((N + 7) / 8)), dim3(kThreads), 0, y, ep, none,
                              w, N, K, 1.0f);
-      case Fp8Shape::kR4U2:
-        return launch_kernel(c, true, k_fp8_gemv<16, kRows, 2, kThreads, false, true>, g,
-                             dim3(kThreads), 0, y, ep, none, w, N, K, 1.0f);
       default:
         return launch_kernel(c, true, k_fp8_gemv<16, kRows, 4, kThreads, false, true>, g,
                              dim3(kThreads), 0, y, ep, none, w, N, K, 1.0f);
