@@ -37,15 +37,17 @@
 //                 written by TMA (TMEM is free again before the stores land),
 //                 otherwise directly with bounds guards.
 //   warps 2, 3    idle.
-// Pair tiles (the plain FP8 / NVFP4 GEMM with M > 128): a cluster of two CTAs
-// on two SMs shares a tile of 512 A rows x 256 weight rows.  Each CTA loads
-// 256 A rows and 128 weight rows and decodes only those; the even CTA's MMA
-// thread issues tcgen05.mma.cta_group::2 (M = 256: 128 rows from each CTA's
-// A, N = 256: 128 weight rows from each CTA) and each CTA's TMEM receives the
-// sums of its own rows.  The weight bytes a CTA moves through shared memory
-// per K step halve for the same MMA work; the odd CTA's dequant and epilogue
-// warps signal the even CTA's barriers remotely, and the MMA's commits reach
-// both CTAs' barriers (multicast).
+// Pair tiles (the plain FP8 / NVFP4 GEMM with M > 128, W8A8 with M > 128 and
+// K <= 16320, any-K FP8 with M > 256; the grouped GEMMs keep one-CTA tiles):
+// a cluster of two CTAs on two SMs shares a tile of 512 A rows (W8A8: 256)
+// x 256 weight rows.  Each CTA loads its A rows and 128 weight rows and
+// decodes only those; the even CTA's MMA thread issues
+// tcgen05.mma.cta_group::2 (M = 256: 128 rows from each CTA's A, N = 256:
+// 128 weight rows from each CTA) and each CTA's TMEM receives the sums of
+// its own rows.  The weight bytes a CTA moves through shared memory per K
+// step halve for the same MMA work; the odd CTA's dequant and epilogue warps
+// signal the even CTA's barriers remotely, and the MMA's commits reach both
+// CTAs' barriers (multicast).
 // W8A8 (Fmt::kInt8): the A tile is int8 too and holds 128 rows.  The page's
 // int32 accumulation is kept exact on binary16 MMAs by splitting every A code
 // into two base-16 digits, a = 16 h + l (h in [-8, 8], l in [-8, 7]): the
