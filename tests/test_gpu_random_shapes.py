@@ -4,7 +4,8 @@ Each case draws its sizes, output type and epilogue from a fixed seed, so a
 failure names a reproducible case.  Sizes stay small enough for the float64
 oracle (a few hundred rows and columns) but cover ragged M, N and K (odd K
 for the FP8 calls), the few-row and general GEMM kernels, and grouped calls
-with empty, -1 and out-of-range groups.
+with empty, -1 and out-of-range groups; M up to 1100 reaches several CTA-pair
+tiles.
 """
 
 import numpy as np
@@ -38,11 +39,11 @@ def _check(got, pre, tol_pre, bias64, act, out_dtype, what):
     assert_within(got, ref, oracle.tolerance_epilogue(tol_pre, ref, act, OUT_KIND[out_dtype]), what)
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(16))
 def test_random_fp8_matmul(case):
     lib()
     rng = np.random.default_rng(1000 + case)
-    m = int(rng.choice([1, 2, 7, 16, 64, 127, 128, 129, 300, 513]))
+    m = int(rng.choice([1, 2, 7, 16, 64, 127, 128, 129, 300, 513, 700, 1100]))
     n = int(rng.integers(1, 700))
     k = int(rng.integers(1, 700)) if case % 2 else 16 * int(rng.integers(1, 40))
     out_dtype = OUT[case % 3]
@@ -56,11 +57,11 @@ def test_random_fp8_matmul(case):
            out_dtype, f"fp8_matmul {m}x{n}x{k} {out_dtype} {act}")
 
 
-@pytest.mark.parametrize("case", range(8))
+@pytest.mark.parametrize("case", range(12))
 def test_random_nvfp4_matmul(case):
     lib()
     rng = np.random.default_rng(2000 + case)
-    m = int(rng.choice([1, 5, 16, 100, 128, 129, 257]))
+    m = int(rng.choice([1, 5, 16, 100, 128, 129, 257, 513, 800]))
     n = int(rng.integers(1, 600))
     k = 64 * int(rng.integers(1, 16))
     out_dtype = OUT[case % 3]
@@ -155,7 +156,7 @@ def test_random_w8a8(case):
     lib()
     rng = np.random.default_rng(5000 + case)
     if case < 4:
-        m = int(rng.choice([1, 3, 16, 100, 128, 129, 300]))
+        m = int(rng.choice([1, 3, 16, 100, 128, 129, 300, 600]))
         n = int(rng.integers(1, 600))
         k = 16 * int(rng.integers(1, 40))
     else:   # K past what one CTA sums: split over a cluster
