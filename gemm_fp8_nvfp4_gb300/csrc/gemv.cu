@@ -474,13 +474,15 @@ k_nvfp4_gemv(void* __restrict__ y, Epi ep, const uint16_t* __restrict__ x,
 
 constexpr int kRows = 4;
 
-template <int VEC, int R, int U, int MINB = 7>
+// MINB: CTAs per SM the register budget allows; MINB_OV: the same for the
+// overlap-mode instantiation (which keeps more values live across the wait).
+template <int VEC, int R, int U, int MINB = 7, int MINB_OV = MINB>
 cudaError_t fp8_launch(const Ctx& c, void* y, const Epi& ep, const void* x,
                        const uint8_t* w, int64_t N, int64_t K, float alpha) {
   const int64_t grid = (N + R - 1) / R;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (c.overlap_weights) {
-    return launch_kernel(c, true, k_fp8_gemv<VEC, R, U, kThreads, true, false, MINB>,
+    return launch_kernel(c, true, k_fp8_gemv<VEC, R, U, kThreads, true, false, MINB_OV>,
                          dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, y, ep,
                          static_cast<const uint16_t*>(x), w, N, K, alpha);
   }
@@ -492,13 +494,14 @@ cudaError_t fp8_launch(const Ctx& c, void* y, const Epi& ep, const void* x,
 // Launch shape of the 16-byte-vector FP8 GEMV (also used by its read-floor
 // probe).  A thread with exactly two vectors per row (K = 4096) issues all
 // of its rows' vectors in one batch (U = 2: one memory round trip instead of
-// two), in 8-row CTAs (at most 4 per SM) whose free slots let the next
-// kernel of the stream start its prologue and L2 prefetch while this one
-// drains; alone, 4096 x 4096 takes 4.1-4.5 us instead of 3.5 us and
-// 14336 x 4096 11.6 us instead of 11.0 us with 4-row CTAs, but the three
-// decode shapes in sequence take 26.3 us instead of 26.7 us (4-row CTAs for
-// 14336 x 4096 only; measured back to back on one GPU).  Otherwise
-// (K = 14336) 4-row CTAs take a batch of four vectors, then single ones.
+// two), in 8-row CTAs (96 registers: at most 5 per SM) whose free slots let
+// the next kernel of the stream start its prologue and L2 prefetch while
+// this one drains; alone, 4096 x 4096 takes 4.5-4.8 us instead of 3.5 us and
+// 14336 x 4096 11.3 us instead of 11.0 us with 4-row CTAs, but the three
+// decode shapes in sequence take 26.1 us instead of 26.7 us (4-row CTAs for
+// 14336 x 4096; at most 4 8-row CTAs per SM: 26.3 us; measured back to back
+// on one GPU).  Otherwise (K = 14336) 4-row CTAs take a batch of four
+// vectors, then single ones.
 enum class Fp8Shape { kR4U4, kR8U2 };
 Fp8Shape fp8_shape(const Ctx&, int64_t, int64_t K) {
   return (K / 16 + kThreads - 1) / kThreads == 2 ? Fp8Shape::kR8U2 : Fp8Shape::kR4U4;
@@ -509,7 +512,7 @@ cudaError_t fp8_dispatch(const Ctx& c, void* y, const Epi& ep, const void* x,
                          const uint8_t* w, int64_t N, int64_t K, float alpha) {
   if constexpr (VEC == 16) {
     switch (fp8_shape(c, N, K)) {
-      case Fp8Shape::kR8U2: return fp8_launch<16, 8, 2, 4>(c, y, ep, x, w, N, K, alpha);
+      case Fp8Shape::kR8U2: return fp8_launch<16, 8, 2, 5, 4>(c, y, ep, x, w, N, K, alpha);
       default: return fp8_launch<16, kRows, 4>(c, y, ep, x, w, N, K, alpha);
     }
   }
@@ -529,7 +532,7 @@ cudaError_t launch_gemv_read_floor(const Ctx& c, int format, void* y, const uint
     const auto* none = static_cast<const uint16_t*>(nullptr);
     switch (fp8_shape(c, N, K)) {
       case Fp8Shape::kR8U2:
-        return launch_kernel(c, true, k_fp8_gemv<16, 8, 2, kThreads, false, true, 4>,
+        return launch_kernel(c, true, k_fp8_gemv<16, 8, 2, kThreads, false, true, 5>,
                              dim3(static_cast<unsigned>((N + 7) / 8)), dim3(kThreads), 0, y, ep, none,
                              w, N, K, 1.0f);
       default:
