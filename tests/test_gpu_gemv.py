@@ -91,6 +91,41 @@ def test_fp8_gemv_nan_code_propagates():
     assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.isnan(got[3]) and np.isnan(got[5])
 
 
+@pytest.mark.parametrize("case", ["large", "tiny", "inf", "nan", "exact"])
+def test_fp8_gemv_activations_outside_binary16(case):
+    """Activations far outside the binary16 range (beyond 65504, below its
+    subnormal grid), infinities and NaNs: the oracle's result within the
+    tolerance, and the IEEE specials where the definition has them."""
+    lib()
+    n, k = 1000, 4096
+    codes, scale = synth.fp8_weight(n, k, seed=21)
+    x = synth.bf16_activations(1, k, seed=22).reshape(-1).float()
+    if case == "large":
+        x[[5, 900, 4095]] = torch.tensor([1.0e6, -7.0e4, 3.0e5])
+    elif case == "tiny":
+        x[[0, 17, 2048]] = torch.tensor([3.0e-9, -1.0e-7, 2.5e-30])
+    elif case == "inf":
+        x[77] = float("inf")
+    elif case == "nan":
+        x[1234] = float("nan")
+    x = x.to(torch.bfloat16)
+    got = to_f64(gq.fp8_gemv(x.to(DEV), codes.to(DEV), scale, out_dtype=torch.float32))
+    xb = bits(x)
+    w_hat = oracle.decode_fp8(codes.numpy())
+    ref = oracle.fp8_gemv(xb, codes.numpy(), scale)
+    if case in ("inf", "nan"):
+        assert np.array_equal(np.isnan(got), np.isnan(ref))
+        fin = np.isfinite(ref)
+        assert np.array_equal(got[~fin & ~np.isnan(ref)], ref[~fin & ~np.isnan(ref)])
+        ref, got = ref[fin], got[fin]
+        tol = oracle.tolerance(xb[None, :], w_hat, scale)[0][fin] if fin.any() else None
+        if fin.any():
+            assert_within(got, ref, tol, f"fp8 gemv {case}")
+        return
+    tol = oracle.tolerance(xb[None, :], w_hat, scale)[0]
+    assert_within(got, ref, tol, f"fp8 gemv {case}")
+
+
 def test_fp8_gemv_equals_gemm_row_of_oracle():
     """The GEMV of row i equals row i of the oracle's GEMM (within tolerance)."""
     lib()
