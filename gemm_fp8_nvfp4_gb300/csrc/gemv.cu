@@ -159,17 +159,36 @@ __device__ __forceinline__ float fma_fp8(const uint32_t* words, const float* xf,
 template <int R, int T>
 __device__ __forceinline__ void reduce_and_store(float (&acc)[R], float* red, int64_t row0,
                                                  int64_t N, float alpha, void* y, const Epi& ep) {
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xFFFFFFFFu, acc[r], off);
-  }
+  static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (lane == 0) {
+  // Warp sums of the R rows by a transposed butterfly: while n > 1 values are
+  // live, the xor step with offset o hands half of them to the partner lane
+  // (lanes with bit o set keep the upper half) and adds what comes back, so
+  // the first log2(R) steps move n/2 values each instead of R; the remaining
+  // steps sum one value.  Lane l then holds the warp's sum of row
+  // l / (32 / R), the same in every lane of its group (a fixed order: the
+  // result is deterministic).
+  float v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) red[warp * R + r] = acc[r];
+  for (int r = 0; r < R; ++r) v[r] = acc[r];
+#pragma unroll
+  for (int off = 16, n = R; off > 0; off >>= 1) {
+    if (n > 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+      }
+      n >>= 1;
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], off);
+    }
   }
+  constexpr int kGroup = 32 / R;   // lanes per row after the butterfly
+  if (lane % kGroup == 0) red[warp * R + lane / kGroup] = v[0];
   __syncthreads();
   if (threadIdx.x < R) {
     const int r = threadIdx.x;
