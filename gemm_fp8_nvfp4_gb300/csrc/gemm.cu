@@ -37,8 +37,8 @@
 //                 written by TMA (TMEM is free again before the stores land),
 //                 otherwise directly with bounds guards.
 //   warps 2, 3    idle.
-// Pair tiles (the plain FP8 / NVFP4 GEMM with M > 128, W8A8 with M > 128 and
-// K <= 16320, any-K FP8 with M > 256; the grouped GEMMs keep one-CTA tiles):
+// Pair tiles (the plain FP8 / NVFP4 GEMM with M > 128, W8A8 with M > 128,
+// any-K FP8 with M > 256; the grouped GEMMs keep one-CTA tiles):
 // a cluster of two CTAs on two SMs shares a tile of 512 A rows (W8A8: 256)
 // x 256 weight rows.  Each CTA loads its A rows and 128 weight rows and
 // decodes only those; the even CTA's MMA thread issues
@@ -49,14 +49,16 @@
 // signal the even CTA's barriers remotely, and the MMA's commits reach both
 // CTAs' barriers (multicast).
 // W8A8 (Fmt::kInt8): the A tile is int8 too and holds 128 rows.  The page's
-// int32 accumulation is kept exact on binary16 MMAs by splitting every A code
-// into two base-16 digits, a = 16 h + l (h in [-8, 8], l in [-8, 7]): the
-// dequant warps widen the weight codes and the two digit planes of A exactly
-// to binary16, the two MMA halves of the tile accumulate sum h*b and sum l*b
-// (each partial sum at most 1024 K in magnitude, so exact in float32 while K
-// per CTA <= 16320), and the epilogue forms the int32 sum 16 * H + L before
-// the dequant multiplies by a_scale[m] and b_scale[n].  Longer K is split
-// over a thread-block cluster whose int32 partials are added exactly.
+// int32 accumulation is kept exact on binary16 MMAs: the dequant warps widen
+// both operands' codes exactly to binary16, every product is an integer of
+// magnitude at most 2^14, and the MMAs accumulate chunks of at most
+// kInt8ChunkSteps K steps (1024 K) in float32, where every partial sum is an
+// integer of magnitude at most 2^24 and therefore exact.  At the end of each
+// chunk the epilogue warps convert the chunk's sums to int32 and add them to
+// a running int32 sum kept in the second TMEM accumulator (the MMAs of the
+// next chunk wait for that hand-over); after the tile's last chunk the
+// dequant multiplies by a_scale[m] and b_scale[n].  A split-K cluster adds
+// its CTAs' int32 partials exactly.
 // Tiles are visited m-fastest so that consecutive CTAs share a weight tile
 // through L2 (the pages' Morton raster serves the same purpose).
 //
@@ -103,15 +105,18 @@ constexpr int kWarpMma = 1;
 constexpr int kDeqWarp0 = 4;
 constexpr int kDeqWarps = 8;     // 256 threads: one weight row each
 constexpr int kEpiWarp0 = 12;    // 4 warps: TMEM lane groups 0..3
-constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators (one per A half)
+constexpr int kTmemCols = 512;   // two 256-column fp32 accumulators (one per A half; W8A8:
+                                 // the chunk's float32 sums and the running int32 sums)
 
 constexpr uint32_t kPartStride = BN * 4 + 16;   // split-K partial row: 256 fp32 + pad
-// W8A8: K steps one CTA may sum (255 x 64 = 16320 K; every digit-plane partial
-// sum stays below 1024 x 16320 < 2^24, exact in float32).
-constexpr int kInt8MaxStepsPerCta = 255;
+// W8A8: K steps per float32 chunk.  |code| <= 128, so every product is at
+// most 2^14 and a chunk's partial sums at most 16 * 64 * 2^14 = 2^24 in
+// magnitude: integers that float32 holds exactly.
+constexpr int kInt8ChunkSteps = 16;
+static_assert(static_cast<int64_t>(kInt8ChunkSteps) * BK * 128 * 128 <= (1LL << 24),
+              "W8A8 chunk sums are exact in float32");
+static_assert(kInt8MaxK * 128 * 128 < (1LL << 31), "W8A8 int32 sums cannot overflow");
 constexpr int kMaxClusterSplit = 8;   // K split over at most a portable cluster
-static_assert(static_cast<int64_t>(kInt8MaxStepsPerCta) * BK * 8 == kInt8MaxK,
-              "the C ABI's W8A8 K limit is eight CTAs' worth");
 constexpr uint32_t kABytes = BM * BK * 2;        // 32 KB
 constexpr uint32_t kAHalfBytes = UMMA_M * BK * 2;  // 16 KB: offset of the second A half
 constexpr uint32_t kDeqBytes = BN * BK * 2;      // 32 KB
@@ -236,11 +241,11 @@ template <Fmt F> struct SmemPair {
   static constexpr uint32_t kAlloc = kTotal + 1024;
 };
 // W8A8 pair tiles: 256 output rows (128 per CTA) x 256 weight rows; the
-// decoded stage holds the CTA's 128 weight rows and the two digit planes of
-// its 128 A rows as binary16 (W at +0, high digits at +16 KB, low at +32 KB).
+// decoded stage holds the CTA's 128 weight rows and its 128 A rows as
+// binary16 (W at +0, A at +16 KB).
 template <> struct SmemPair<Fmt::kInt8> {
   static constexpr int kRawSt = 4;
-  static constexpr int kDeqSt = 3;   // 350 us with 2 decoded stages, 337 us with 3
+  static constexpr int kDeqSt = 4;
   static constexpr int kWRows = kPairWRows;
   static constexpr uint32_t kWBytes = RawLayout<Fmt::kInt8>::kWBytes / 2;   // 8 KB
   static constexpr uint32_t kScaleBytes = 0;
@@ -248,7 +253,7 @@ template <> struct SmemPair<Fmt::kInt8> {
   static constexpr uint32_t kAStride = kARawBytes;
   static constexpr bool kADeq = true;
   static constexpr uint32_t kDeqAOff = kDeqBytes / 2;                       // 16 KB
-  static constexpr uint32_t kDeqStride = kDeqBytes / 2 + kABytes;           // 48 KB
+  static constexpr uint32_t kDeqStride = kDeqBytes / 2 + kAHalfBytes;       // 32 KB
   static constexpr uint32_t kDeqOff = 0;
   static constexpr uint32_t kAOff = kDeqOff + kDeqSt * kDeqStride;
   static constexpr uint32_t kWOff = kAOff + kRawSt * kAStride;
@@ -304,11 +309,11 @@ using SmemFor = typename std::conditional<
     typename std::conditional<kPair, SmemPair<F>, Smem<F>>::type>::type;
 
 // W8A8: raw int8 A (8 KB, 128 rows) and W (16 KB) stages, 64-byte swizzle,
-// and decoded stages holding the weight and the two digit planes of A as
-// binary16 (W at +0, A's high digits at +32 KB, low digits at +48 KB).
+// and decoded stages holding the weight and A as binary16 (W at +0, A at
+// +32 KB).
 template <> struct Smem<Fmt::kInt8> {
   static constexpr int kRawSt = kRawStages;
-  static constexpr int kDeqSt = kDeqStages;
+  static constexpr int kDeqSt = 3;
   static constexpr int kWRows = BN;
   static constexpr uint32_t kWBytes = RawLayout<Fmt::kInt8>::kWBytes;
   static constexpr uint32_t kScaleBytes = 0;
@@ -316,13 +321,13 @@ template <> struct Smem<Fmt::kInt8> {
   static constexpr uint32_t kAStride = kARawBytes;
   static constexpr bool kADeq = true;                         // MMA reads A from the decoded stage
   static constexpr uint32_t kDeqAOff = kDeqBytes;
-  static constexpr uint32_t kDeqStride = kDeqBytes + kABytes; // 64 KB
+  static constexpr uint32_t kDeqStride = kDeqBytes + kAHalfBytes;  // 48 KB
   static constexpr uint32_t kDeqOff = 0;
-  static constexpr uint32_t kAOff = kDeqOff + kDeqStages * kDeqStride;
+  static constexpr uint32_t kAOff = kDeqOff + kDeqSt * kDeqStride;
   static constexpr uint32_t kWOff = kAOff + kRawStages * kAStride;
   static constexpr uint32_t kSOff = kWOff + kRawStages * RawLayout<Fmt::kInt8>::kWBytes;
   static constexpr uint32_t kBarOff = kSOff;
-  static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqStages + 4 + 1;
+  static constexpr uint32_t kNumBars = 2 * kRawStages + 2 * kDeqSt + 4 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kStageOff = 0, kStageBytes = 0;   // no TMA-store staging
   static constexpr uint32_t kTotal = kMiscOff + 16;
@@ -496,11 +501,10 @@ __device__ __forceinline__ void prefetch_span_l2(const uint8_t* base, int64_t lo
     tc::bulk_prefetch_l2(base + o, static_cast<uint32_t>(min(kPiece, hi - o)));
 }
 
-// W8A8: the int32 sum 16 H + L from the float32 accumulators of the high and
-// low digit planes (both hold exact integers below 2^24, so the conversions
-// are exact; |16 H + L| <= 128 * 128 * K fits int32 for the K the host allows).
-__device__ __forceinline__ int digit_sum(uint32_t hi_bits, uint32_t lo_bits) {
-  return 16 * __float2int_rz(__uint_as_float(hi_bits)) + __float2int_rz(__uint_as_float(lo_bits));
+// W8A8: a chunk's float32 sum (an exact integer of magnitude <= 2^24, so the
+// conversion is exact) plus the running int32 sum of the earlier chunks.
+__device__ __forceinline__ int chunk_sum(uint32_t chunk_bits, uint32_t run_bits, bool have_run) {
+  return __float2int_rz(__uint_as_float(chunk_bits)) + (have_run ? static_cast<int>(run_bits) : 0);
 }
 
 // ----------------------------------------------------------------- kernel --
@@ -539,9 +543,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   if (threadIdx.x == 0) {
     // The raw stage is full after the copies (+ the NVFP4 scale copies).  It
     // is empty after the MMA (+ the dequant warps that read its raw weight;
-    // any K: the loader warps finish with a stage before the MMA starts).
+    // any K: the loader warps finish with a stage before the MMA starts;
+    // W8A8: the MMA reads only decoded stages, so the dequant warps alone).
     constexpr uint32_t kRawArrivals = (kAnyK || F == Fmt::kNvfp4) ? 1 + 32 : 1;
-    constexpr uint32_t kRawReleases = kAnyK ? 1 : 1 + kDeqWarps;
+    constexpr uint32_t kRawReleases = kAnyK ? 1 : F == Fmt::kInt8 ? kDeqWarps : 1 + kDeqWarps;
     // Pair tiles: the even CTA's full_deq and tmem_empty also count the odd
     // CTA's dequant and epilogue warps (remote arrivals); the MMA's commits
     // reach the barriers of both CTAs.
@@ -604,9 +609,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   // the offset of its A rows within each 256-row half of the tile.
   const int w_row0 = kPair ? prank * kPairWRows : 0;
   const int a_row0 = kPair ? prank * (kAnyK ? BM : UMMA_M) : 0;
-  // (W8A8: the two MMA halves are the digit planes of the same rows.  Any
-  // K: CTA r holds tile rows 256 r + [0, 256) -- in residue order, or in
-  // order as halves of 128 -- and both halves are always issued.)
+  // (W8A8: one MMA half of 128 rows per CTA; the second accumulator holds
+  // the running int32 sums.  Any K: CTA r holds tile rows 256 r + [0, 256)
+  // -- in residue order, or in order as halves of 128 -- and both halves are
+  // always issued.)
   constexpr int kHalfRows = (kPair && F != Fmt::kInt8 && !kAnyK) ? 2 * UMMA_M : UMMA_M;   // tile rows per MMA half
   const int kb0 = split ? crank * p.kb_per_split : 0;
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
@@ -823,67 +829,79 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     constexpr int kMmaM = kPair ? 2 * UMMA_M : UMMA_M;
     constexpr uint32_t kIdesc =
         F == Fmt::kInt8 ? tc::idesc_f16_f32(kMmaM, BN) : tc::idesc_bf16_f32(kMmaM, BN);
+    // Hand-overs of the accumulators to the epilogue: one per tile (W8A8:
+    // one per chunk of at most kInt8ChunkSteps K steps, whose first MMA
+    // starts a fresh float32 sum).
+    constexpr int kChunk = F == Fmt::kInt8 ? kInt8ChunkSteps : (1 << 30);
     int s = 0, d = 0;
     uint32_t ph = 0, dph = 0;
-    int it = 0;
+    int hand = 0;
     bool ok = true;
     for (int t = t_first; t < total_tiles && ok; t += t_step) {
       const Tile tl = get_tile<kGrouped>(p, t);
       if (!tl.valid || tl.expert < 0) continue;
-      const uint32_t acc_ph = it & 1;
-      ++it;
       // (Any K: the rows are in residue order, spread over both halves.)
-      // (W8A8: the halves are the two digit planes of the tile's 128 rows.)
-      const bool two_halves = F == Fmt::kInt8 || (kAnyK && !p.a_tma) || tl.m_end - tl.m0 > kHalfRows;
-      // Both accumulators free (the epilogue of the previous tile has read them).
-      if (!tc::mbar_wait<kPair>(&tmem_empty[0], acc_ph ^ 1, abort_flag, p.status, kStatusTimeoutMma)) break;
-      tc::tc_fence_after();
-      for (int kb = kb0; kb < nkb; ++kb) {
-        if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma) ||
-            !tc::mbar_wait<kPair>(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
+      // (W8A8: one MMA per K slice; the second accumulator is the epilogue's.)
+      const bool two_halves =
+          F != Fmt::kInt8 && ((kAnyK && !p.a_tma) || tl.m_end - tl.m0 > kHalfRows);
+      for (int cb = kb0; cb < nkb && ok; cb += kChunk) {
+        const int ce = nkb - cb > kChunk ? cb + kChunk : nkb;
+        // The accumulators are free: the epilogue has read the previous hand-over.
+        if (!tc::mbar_wait<kPair>(&tmem_empty[0], (hand & 1) ^ 1, abort_flag, p.status, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_addr = L::kADeq ? smem_base + L::kDeqOff + d * L::kDeqStride + L::kDeqAOff
-                                           : smem_base + L::kAOff + s * L::kAStride;
-          const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
+        for (int kb = cb; kb < ce; ++kb) {
+          // (W8A8: both operands come from the decoded stage; the raw ring is
+          // the dequant warps' alone and may run ahead of the MMAs.)
+          if ((F != Fmt::kInt8 && !tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutMma)) ||
+              !tc::mbar_wait<kPair>(&full_deq[d], dph, abort_flag, p.status, kStatusTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = L::kADeq ? smem_base + L::kDeqOff + d * L::kDeqStride + L::kDeqAOff
+                                             : smem_base + L::kAOff + s * L::kAStride;
+            const uint32_t b_addr = smem_base + L::kDeqOff + d * L::kDeqStride;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
-            const uint64_t a0 = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
-            const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
-            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-            // A tile with at most 128 rows (pair tiles: 256; the ragged end
-            // of M or of a group) needs only the first half; the second
-            // accumulator is unused.
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint64_t bd = tc::sw128_kmajor_desc(b_addr + kk * UMMA_K * 2);
+              const uint64_t a0 = tc::sw128_kmajor_desc(a_addr + kk * UMMA_K * 2);
+              const uint64_t a1 = tc::sw128_kmajor_desc(a_addr + kAHalfBytes + kk * UMMA_K * 2);
+              const uint32_t accum = (kb > cb || kk > 0) ? 1u : 0u;
+              // A tile with at most 128 rows (pair tiles: 256; the ragged end
+              // of M or of a group) needs only the first half; the second
+              // accumulator is unused.
+              if constexpr (kPair) {
+                tc::mma_bf16_pair(tmem_base, a0, bd, kIdesc, accum);
+                if (two_halves) tc::mma_bf16_pair(tmem_base + BN, a1, bd, kIdesc, accum);
+              } else {
+                tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
+                if (two_halves) tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
+              }
+            }
             if constexpr (kPair) {
-              tc::mma_bf16_pair(tmem_base, a0, bd, kIdesc, accum);
-              if (two_halves) tc::mma_bf16_pair(tmem_base + BN, a1, bd, kIdesc, accum);
+              if constexpr (F != Fmt::kInt8) tc::mma_commit_pair(&empty_raw[s], 3);
+              tc::mma_commit_pair(&empty_deq[d], 3);
             } else {
-              tc::mma_bf16(tmem_base, a0, bd, kIdesc, accum);
-              if (two_halves) tc::mma_bf16(tmem_base + BN, a1, bd, kIdesc, accum);
+              if constexpr (F != Fmt::kInt8) tc::mma_commit(&empty_raw[s]);
+              tc::mma_commit(&empty_deq[d]);
             }
           }
-          if constexpr (kPair) {
-            tc::mma_commit_pair(&empty_raw[s], 3);
-            tc::mma_commit_pair(&empty_deq[d], 3);
-          } else {
-            tc::mma_commit(&empty_raw[s]);
-            tc::mma_commit(&empty_deq[d]);
-          }
+          __syncwarp();
+          if (++s == L::kRawSt) { s = 0; ph ^= 1; }
+          if (++d == L::kDeqSt) { d = 0; dph ^= 1; }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if constexpr (kPair) tc::mma_commit_pair(&tmem_full[0], 3);
+          else tc::mma_commit(&tmem_full[0]);
         }
         __syncwarp();
-        if (++s == L::kRawSt) { s = 0; ph ^= 1; }
-        if (++d == L::kDeqSt) { d = 0; dph ^= 1; }
+        ++hand;
       }
-      if (!ok) break;
-      if (lane == 0) {
-        if constexpr (kPair) tc::mma_commit_pair(&tmem_full[0], 3);
-        else tc::mma_commit(&tmem_full[0]);
-      }
-      __syncwarp();
     }
     // Drain: every MMA issued by this thread completes before TMEM is freed.
     if (lane == 0) {
@@ -1027,12 +1045,12 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         if constexpr (F == Fmt::kInt8) {
           // Rows of 64 int8 codes (TMA 64-byte swizzle: chunk c at
           // c ^ ((row >> 1) & 3)) -> binary16, exactly: weight row `row`
-          // (pair tiles: half of its chunks), and decoded A row `tid` =
-          // digit tid >> 7 (0: high, 1: low) of A row tid & 127.
+          // (pair tiles: half of its chunks), and half of the chunks of A
+          // row tid & 127 (chunks 2 (tid >> 7) and 2 (tid >> 7) + 1).
           const uint32_t a_raw = smem_base + L::kAOff + s * L::kAStride;
           const uint32_t a_dq = b_addr + L::kDeqAOff;
           const int ar = tid & (UMMA_M - 1);
-          const int digit = tid >> 7;
+          const int apart = tid >> 7;
 #pragma unroll
           for (int i = 0; i < 4 / kParts; ++i) {
             const int c = part * (4 / kParts) + i;
@@ -1043,12 +1061,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
             tc::sts128(b_addr + sw128_off(row, 2 * c + 1), hi);
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 2; ++i) {
+            const int c = 2 * apart + i;
             uint4 lo, hi;
             const uint32_t asrc = ar * 64 + ((c ^ ((ar >> 1) & 3)) << 4);
-            s8x16_digit_to_f16(tc::lds128(a_raw + asrc), digit, lo, hi);
-            tc::sts128(a_dq + sw128_off(tid, 2 * c), lo);
-            tc::sts128(a_dq + sw128_off(tid, 2 * c + 1), hi);
+            s8x16_to_f16(tc::lds128(a_raw + asrc), lo, hi);
+            tc::sts128(a_dq + sw128_off(ar, 2 * c), lo);
+            tc::sts128(a_dq + sw128_off(ar, 2 * c + 1), hi);
           }
         } else if constexpr (F == Fmt::kFp8) {
           // Row of 64 codes, TMA 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3).
@@ -1094,7 +1113,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   } else if (warp >= kEpiWarp0) {
     // --------------------------------------------------------- epilogue --
     const int g = warp & 3;                 // TMEM lane group of this warp
-    int it = 0;
+    int hand = 0;                           // accumulator hand-overs received
     const uint32_t stage = smem_base + L::kStageOff + g * 4096;   // this warp's 2 staging boxes
     int sbuf = 0;
     for (int t = t_first; t < total_tiles; t += t_step) {
@@ -1121,48 +1140,83 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         }
         continue;
       }
-      const uint32_t acc_ph = it & 1;
-      ++it;
-      if (!tc::mbar_wait<kPair>(&tmem_full[0], acc_ph, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
-      tc::tc_fence_after();
+      // W8A8: every chunk, the tile's last included, is added to the running
+      // int32 sums in the second accumulator (lane 32 g + lane, columns
+      // BN + c) and the first accumulator is handed back to the MMAs; the
+      // output is then formed from the int32 sums while the MMAs run the
+      // next tile.
+      if constexpr (F == Fmt::kInt8) {
+        const int nch = (nkb - kb0 + kInt8ChunkSteps - 1) / kInt8ChunkSteps;
+        const uint32_t lrow = tmem_base + (static_cast<uint32_t>(g * 32) << 16);
+        bool fail = false;
+        bool have_run = false;
+#pragma unroll 1
+        for (int j = 0; j < nch; ++j) {
+          if (!tc::mbar_wait<kPair>(&tmem_full[0], hand & 1, abort_flag, p.status, kStatusTimeoutEpilogue)) {
+            fail = true;
+            break;
+          }
+          ++hand;
+          tc::tc_fence_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32], y[32];
+            tc::tmem_ld_32x32b_x32(lrow + c0, r);
+            if (have_run) tc::tmem_ld_32x32b_x32(lrow + BN + c0, y);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = static_cast<uint32_t>(chunk_sum(r[i], have_run ? y[i] : 0u, have_run));
+            tc::tmem_st_32x32b_x32(lrow + BN + c0, y);
+          }
+          tc::tmem_wait_st();
+          have_run = true;
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&tmem_empty[0]), 0));
+            else tc::mbar_arrive(&tmem_empty[0]);
+          }
+        }
+        if (fail) break;
+      } else {
+        if (!tc::mbar_wait<kPair>(&tmem_full[0], hand & 1, abort_flag, p.status, kStatusTimeoutEpilogue)) break;
+        ++hand;
+        tc::tc_fence_after();
+      }
       if (split) {
         // This CTA's raw fp32 partial of rows [0, 128) -> shared memory (the
         // operand rings are idle now: every MMA has completed).  Rows are
         // padded to kPartStride bytes so that 8 consecutive rows hit
         // distinct banks.  The cluster reduction at the end of the kernel sums
         // the partials of all ranks.
-        // W8A8: the partial is the exact int32 sum 16 H + L of the two digit
-        // planes' accumulators (bits stored; the reduction adds int32).
+        // W8A8: the partial is the exact int32 sum in the second
+        // accumulator (bits stored; the reduction adds int32).
         const int r_local = g * 32 + lane;
         const uint32_t prow = smem_base + r_local * kPartStride;
+        constexpr uint32_t kAccCol = F == Fmt::kInt8 ? BN : 0;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + c0, r);
+          tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + kAccCol + c0, r);
           tc::tmem_wait_ld();
-          if constexpr (F == Fmt::kInt8) {
-            uint32_t rl[32];
-            tc::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(g * 32) << 16) + BN + c0, rl);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(digit_sum(r[i], rl[i]));
-          }
           if (tl.m0 + r_local < tl.m_end) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               tc::sts128(prow + (c0 + 4 * i) * 4, make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]));
           }
         }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
+        if constexpr (F != Fmt::kInt8) {
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tmem_empty[0]);
+        }
         continue;
       }
       const bool plain_epi = epi_plain(p.ep);
       const bool vec_ok = p.ep.out_kind == kOutF32 ? (p.N % 4 == 0) : (p.N % 8 == 0);
       const int64_t bias0 = static_cast<int64_t>(tl.expert) * p.ep.bias_stride;   // bias row of the expert
       const bool residue_rows = kAnyK && !p.a_tma;
-      // W8A8: one half of output rows (the TMEM halves are its digit planes).
+      // W8A8: one half of output rows, from the int32 sums in the second accumulator.
       const int halves = F == Fmt::kInt8 ? 1 : (residue_rows || tl.m_end - tl.m0 > kHalfRows) ? 2 : 1;
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
@@ -1176,24 +1230,20 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(taddr + c0, r);
+          tc::tmem_ld_32x32b_x32(taddr + (F == Fmt::kInt8 ? BN : 0) + c0, r);
           tc::tmem_wait_ld();
           const int n = tl.n0 + c0;
           float v[32];
           if constexpr (F == Fmt::kInt8) {
-            // acc = 16 H + L exactly in int32 (the low-digit plane is the
-            // second TMEM half), then (float(acc) * a_scale[m]) * b_scale[n],
-            // each step rounded once; lane i loads b_scale of column n + i and
-            // the warp shares it (every lane of the warp is here: the row test
-            // comes after).
-            uint32_t rl[32];
-            tc::tmem_ld_32x32b_x32(taddr + BN + c0, rl);
-            tc::tmem_wait_ld();
+            // acc = the exact int32 sum, then (float(acc) * a_scale[m]) *
+            // b_scale[n], each step rounded once; lane i loads b_scale of
+            // column n + i and the warp shares it (every lane of the warp is
+            // here: the row test comes after).
             const float sbv = n + lane < p.N ? __ldg(p.b_scale + n + lane) : 0.f;
             const float sa = row_ok ? __ldg(p.a_scale + m) : 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              v[i] = __fmul_rn(__fmul_rn(__int2float_rn(digit_sum(r[i], rl[i])), sa),
+              v[i] = __fmul_rn(__fmul_rn(__int2float_rn(static_cast<int>(r[i])), sa),
                                __shfl_sync(0xFFFFFFFFu, sbv, i));
           }
           // TMA store of the warp's 32 x 32 box (16-bit outputs, all rows of
@@ -1268,11 +1318,13 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           }
         }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&tmem_empty[0]), 0));
-        else tc::mbar_arrive(&tmem_empty[0]);
+      if constexpr (F != Fmt::kInt8) {   // (W8A8 handed the accumulator back after its last chunk)
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(&tmem_empty[0]), 0));
+          else tc::mbar_arrive(&tmem_empty[0]);
+        }
       }
     }
     // Every TMA store of this warp has completed before the CTA exits.
@@ -1574,7 +1626,7 @@ cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_
   // K = 0: every sum is 0, so the output is the epilogue of 0.
   if (K == 0) return fill_zero(c, out, ep, M * N, N, 0.f);
   if (K > kInt8MaxK) return cudaErrorInvalidValue;   // refused earlier by the C ABI
-  if (M > UMMA_M && (K + BK - 1) / BK <= kInt8MaxStepsPerCta) {
+  if (M > UMMA_M) {
     // Pair tiles: 256 output rows (128 A rows per CTA) x 256 weight rows.
     CUtensorMap ta, tw;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, BK, UMMA_M, CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -1597,21 +1649,7 @@ cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_
   p.a_scale = a_scale;
   p.b_scale = b_scale;
   const int tiles = ((p.M + UMMA_M - 1) / UMMA_M) * p.num_n_tiles;
-  int grid;
-  if (p.num_k_blocks <= kInt8MaxStepsPerCta) {
-    grid = plan_split(c, p, tiles);
-  } else {
-    // Each CTA's digit-plane sums stay exact only over at most
-    // kInt8MaxStepsPerCta K steps: split K over a cluster of 2, 4 or 8 CTAs
-    // (the column slices of the reduction need BN / S % 4 == 0), whose int32
-    // partials the cluster adds exactly.
-    int sp = 2;
-    while ((p.num_k_blocks + sp - 1) / sp > kInt8MaxStepsPerCta) sp *= 2;
-    if (sp > 8) return cudaErrorInvalidValue;
-    p.ksplit = sp;
-    p.kb_per_split = (p.num_k_blocks + sp - 1) / sp;
-    grid = tiles * sp;
-  }
+  const int grid = plan_split(c, p, tiles);
   return launch<Fmt::kInt8, false>(c, ta, tw, nullptr, p, grid);
 }
 

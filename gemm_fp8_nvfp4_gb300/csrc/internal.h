@@ -87,7 +87,7 @@ cudaError_t launch_fp8_grouped_gemm(const Ctx& c, void* out, const Epi& ep,
                                     int64_t total_M, int64_t N, int64_t K);
 
 // W8A8: c = epilogue((acc * a_scale[m]) * b_scale[n]), acc = sum a[m,k] b[n,k]
-// exactly in int32, for K <= kInt8MaxK (eight CTAs of 255 K steps of 64).
+// exactly in int32, for K <= kInt8MaxK (128 * 128 * kInt8MaxK < 2^31).
 constexpr int64_t kInt8MaxK = 130560;
 cudaError_t launch_int8_gemm(const Ctx& c, void* out, const Epi& ep, const int8_t* a,
                              const int8_t* b, const float* a_scale, const float* b_scale,

@@ -308,14 +308,13 @@ int gq_int8_quantize_rows(int8_t* q, float* scale, const void* x, int64_t M, int
  *   any codes).  a, b, c 16-byte aligned; scales 4-byte aligned.
  * acc is the exact int32 sum for every input, as on the page.  GB300 has no
  * int8 tensor-core instruction on sm_103a (tcgen05 kind::i8 is not
- * available there), so the sums run on binary16 tensor-core products: each
- * code of a is split into two base-16 digits, a = 16 h + l with h in [-8, 8]
- * and l in [-8, 7], the weight codes and both digit planes are widened
- * exactly to binary16, the two float32 sums H = sum h b and L = sum l b are
- * exact (every partial sum is an integer below 1024 K per CTA <= 2^24), and
- * acc = 16 H + L is formed in int32.  K beyond 16320 is split over a
- * thread-block cluster of 2, 4 or 8 CTAs whose int32 partials are added
- * exactly.  acc is converted to float32 with round-to-nearest-even.
+ * available there), so the sums run on binary16 tensor-core products: both
+ * operands' codes are widened exactly to binary16, every product is an
+ * integer of magnitude at most 2^14, the products of each chunk of at most
+ * 1024 K are summed in float32 (every partial sum is an integer of magnitude
+ * at most 2^24, so exact), and the chunks are added in int32.  With small M,
+ * K may be split over a thread-block cluster of CTAs whose int32 partials
+ * are added exactly.  acc is converted to float32 with round-to-nearest-even.
  */
 int gq_int8_matmul(void* c, int out_dtype, const int8_t* a, const int8_t* b,
                    const float* a_scale, const float* b_scale, int64_t M, int64_t N,

@@ -159,7 +159,7 @@ def test_random_w8a8(case):
         m = int(rng.choice([1, 3, 16, 100, 128, 129, 300, 600]))
         n = int(rng.integers(1, 600))
         k = 16 * int(rng.integers(1, 40))
-    else:   # K past what one CTA sums: split over a cluster
+    else:   # long K: many float32 chunks added in int32 (small M: a split-K cluster)
         m = int(rng.choice([1, 3, 16, 100]))
         n = int(rng.integers(1, 200))
         k = 16 * int(rng.integers(1021, 2600))
@@ -172,6 +172,5 @@ def test_random_w8a8(case):
     out_dtype = OUT[case % 3]
     c = gq.int8_matmul(qa, qb.to(DEV), sa, sb.to(DEV), out_dtype=out_dtype)
     pre = oracle.int8_matmul(want_q, qb.numpy(), want_s, sb.numpy()).astype(np.float64)
-    # the sums are exact int32 (cases 4 and 5: K > 16320, split over a
-    # cluster), so only the output rounding separates the two
+    # the sums are exact int32, so only the output rounding separates the two
     _check(to_f64(c), pre, np.zeros_like(pre), None, "none", out_dtype, f"w8a8 {m}x{n}x{k}")

@@ -3,8 +3,9 @@ oracle.
 
 The quantizer takes its integer decisions in float32 like the oracle, so codes
 and scales are compared bit for bit.  The GEMM's sum is the page's exact int32
-accumulation for every input (the kernel sums base-16 digit planes of A,
-each exactly, and forms 16 H + L in int32), so the float32 dequant
+accumulation for every input (the kernel sums chunks of at most 1024 K on
+binary16 tensor-core products, each chunk exactly in float32, and adds the
+chunks in int32), so the float32 dequant
 ((float32(acc) * a_scale) * b_scale, then bias) and the output rounding match
 the oracle bit for bit, including sums far beyond 2^24.  Only an activation
 adds tolerance: its float32 evaluation against the oracle's float64 one.
@@ -194,12 +195,15 @@ def extreme_codes(m, k, seed):
 
 
 @pytest.mark.parametrize("m,n,k", [(130, 256, 4096), (5, 300, 16320), (3, 64, 16384),
-                                   (129, 260, 24576), (2, 40, 65536), (3, 8, 130560)])
+                                   (129, 260, 24576), (2, 40, 65536), (3, 8, 130560),
+                                   (257, 256, 1024), (300, 256, 1040), (129, 128, 2048),
+                                   (4, 64, 1024), (6, 48, 3072), (260, 16, 130560)])
 def test_int8_extreme_codes_exact(m, n, k):
-    """All codes at +-127 / -128, K from 4096 (one CTA; 127^2 * 4096 ~ 2^26)
-    through 16320 (the longest K one CTA sums) and 16384 (split over a
-    cluster of 2) up to 130560 (8 CTAs, sums near 2^31): bit-exact against
-    the exact int32 sums of the oracle."""
+    """All codes at +-127 / -128 (every chunk of 1024 K reaches the float32
+    exact limit 2^24), K from one chunk (1024) and a chunk plus one 16-K step
+    (1040) through 4096 (127^2 * 4096 ~ 2^26) up to 130560 (sums near 2^31),
+    on CTA pairs (M > 128) and on one-CTA tiles with and without a split-K
+    cluster: bit-exact against the exact int32 sums of the oracle."""
     lib()
     qa = extreme_codes(m, k, seed=m + k)
     qb = extreme_codes(n, k, seed=n + 3 * k)
