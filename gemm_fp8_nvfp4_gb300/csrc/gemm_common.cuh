@@ -60,33 +60,6 @@ __device__ __forceinline__ void s8x16_to_f16(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// 16 int8 codes a -> one of their two base-16 digits as 16 binary16, exactly:
-// a = 16 h + l with h = floor((a + 8) / 16) in [-8, 8] and l in [-8, 7]
-// (digit 0: h, digit 1: l).  With u = a + 128 (the sign bit flipped) per
-// byte, h + 8 = (u + 8) >> 4 and l + 8 = (u + 8) & 15, formed bytewise with
-// no carry between bytes; each becomes the low byte of the binary16
-// 1024 + d and 1032 is subtracted (exact).  Every |digit x code| is at most
-// 8 x 128 = 1024, so a float32 sum of up to 16383 such products holds every
-// partial sum exactly.
-__device__ __forceinline__ void s8x16_digit_to_f16(uint4 v, int digit, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t u = w[i] ^ 0x80808080u;
-    const uint32_t t = (u & 0x0F0F0F0Fu) + 0x08080808u;            // (u & 15) + 8 per byte, <= 23
-    const uint32_t d = digit == 0 ? ((u >> 4) & 0x0F0F0F0Fu) + ((t >> 4) & 0x01010101u)
-                                  : t & 0x0F0F0F0Fu;
-    uint32_t h0, h1;
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(h0) : "r"(d), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x5342;" : "=r"(h1) : "r"(d), "r"(0x64646464u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i]) : "r"(h0), "r"(0x64086408u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i + 1]) : "r"(h1), "r"(0x64086408u));
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
 // 8 packed bytes (16 E2M1 codes, low nibble first) x one E4M3 block scale
 // (given as f16 bits) -> 16 bf16, exact (the product has at most 6
 // significant bits and lies in [2^-10, 2688]).
