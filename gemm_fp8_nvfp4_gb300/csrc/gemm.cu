@@ -64,9 +64,10 @@
 //
 // Any K (FP8 only; the "fp4_matmul" page's K-strip plus tail loop): when K is
 // not a multiple of 16 the rows of A (2K bytes) and W (K bytes) are not
-// 16-byte strided, but rows 8 apart in A and 16 apart in W are (16K bytes).
-// So A is described as [M/8 groups, 8K elements] and W as [N/16 groups, 16K
-// bytes]: one TMA box per residue class (row mod 8, row mod 16) brings the
+// 16-byte strided, but rows 8 apart in A (16K bytes) and R = 16 / gcd(K, 16)
+// apart in W (RK bytes; R = 2 when K % 16 == 8) are.  So A is described as
+// [M/8 groups, 8K elements] and W as [N/R groups, RK bytes]: one TMA box per
+// residue class (row mod 8, row mod R) brings the
 // 16-byte-aligned windows around the stage's K range of every row of that
 // class (rows of an incomplete last group come by cp.async).  The dequant
 // warps then shift each row by its fixed misalignment, zero the K tail, and
@@ -176,7 +177,7 @@ constexpr uint32_t kAnyRowA = 144;                 // raw A window bytes per row
 constexpr uint32_t kAnyRowW = 80;                  // raw weight window bytes per row
 constexpr int kAnyInTile = 28;                     // A box rows that land in place
 constexpr uint32_t kAnySideSlot = 640;             // 4 x 144 bytes, rounded to 128
-constexpr uint32_t kAnyWBox = 16 * kAnyRowW;       // 1280: W box of one residue
+constexpr uint32_t kAnyWArea = BN * kAnyRowW;      // raw W windows of a tile's 256 weight rows
 static_assert(kAnyInTile * kAnyRowA <= 32 * BK * 2, "in-place A rows fit their 4 KB");
 struct SmemAnyK {
   static constexpr int kRawSt = 2;
@@ -188,7 +189,7 @@ struct SmemAnyK {
   static constexpr uint32_t kDeqOff = kABytes;
   static constexpr uint32_t kSideOff = kABytes + kDeqBytes;
   static constexpr uint32_t kWOff = kSideOff + 8 * kAnySideSlot;
-  static constexpr uint32_t kPartAOff = kWOff + 16 * kAnyWBox;       // <= 7 rows of A
+  static constexpr uint32_t kPartAOff = kWOff + kAnyWArea;           // <= 7 rows of A
   static constexpr uint32_t kPartWOff = kPartAOff + 1024;             // <= 15 rows of W
   static constexpr uint32_t kStage = (kPartWOff + 1280 + 1023) & ~1023u;
   static constexpr uint32_t kAStride = kStage;
@@ -204,7 +205,7 @@ struct SmemAnyK {
   static constexpr uint32_t kAlloc = kTotal + 1024;
   // Transaction bytes of one stage's boxes.
   static constexpr uint32_t kABoxBytes = 8 * 32 * kAnyRowA;
-  static constexpr uint32_t kWBoxBytes = 16 * kAnyWBox;
+  static constexpr uint32_t kWBoxBytes = kAnyWArea;
 };
 
 // Pair tiles (cta_group::2): the two CTAs of a cluster pair share a tile of
@@ -271,9 +272,8 @@ static_assert(SmemPair<Fmt::kFp8>::kAlloc <= 232448 && SmemPair<Fmt::kNvfp4>::kA
 
 // Any-K pair tiles: each CTA realigns its 256 rows of A (tile rows
 // 256 rank + [0, 256), residue order as SmemAnyK) and decodes 128 weight rows
-// (residue boxes of 8 groups of 16 rows); three stages.
-constexpr int kAnyPairWGroups = 8;
-constexpr uint32_t kAnyPairWBox = kAnyPairWGroups * kAnyRowW;   // 640: W box of one residue
+// (one box per W residue class); three stages.
+constexpr uint32_t kAnyPairWArea = kPairWRows * kAnyRowW;   // raw W windows of a CTA's 128 rows
 struct SmemAnyKPair {
   static constexpr int kRawSt = 3;
   static constexpr int kDeqSt = 3;
@@ -284,7 +284,7 @@ struct SmemAnyKPair {
   static constexpr uint32_t kDeqOff = kABytes;
   static constexpr uint32_t kSideOff = kABytes + kDeqBytes / 2;
   static constexpr uint32_t kWOff = kSideOff + 8 * kAnySideSlot;
-  static constexpr uint32_t kPartAOff = kWOff + 16 * kAnyPairWBox;     // <= 7 rows of A
+  static constexpr uint32_t kPartAOff = kWOff + kAnyPairWArea;         // <= 7 rows of A
   static constexpr uint32_t kPartWOff = kPartAOff + 1024;              // <= 15 rows of W
   static constexpr uint32_t kStage = (kPartWOff + 1280 + 1023) & ~1023u;
   static constexpr uint32_t kAStride = kStage;
@@ -299,7 +299,7 @@ struct SmemAnyKPair {
   static constexpr uint32_t kTotal = kMiscOff + 16;
   static constexpr uint32_t kAlloc = kTotal + 1024;
   static constexpr uint32_t kABoxBytes = SmemAnyK::kABoxBytes;
-  static constexpr uint32_t kWBoxBytes = 16 * kAnyPairWBox;
+  static constexpr uint32_t kWBoxBytes = kAnyPairWArea;
 };
 static_assert(SmemAnyKPair::kAlloc <= 232448, "any-K pair stages fit in shared memory");
 
@@ -357,7 +357,8 @@ struct Problem {
   int num_n_tiles;
   int num_k_blocks;
   int G, E, max_rows;          // grouped only
-  int a_groups, w_groups;      // any-K path: full 8-row groups of A, 16-row groups of W
+  int a_groups, w_groups;      // any-K path: full 8-row groups of A, w_res-row groups of W
+  int w_res;                   // any-K path: W rows per 16-byte-strided group, 16 / gcd(K, 16)
   int tma_out;                 // 16-bit output stored through the output tensor map
   int a_tma;                   // any-K path with K % 8 == 0: A by the plain tiled map
   Epi ep;                      // output type and fused epilogue
@@ -709,16 +710,17 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   } else if (kAnyK && warp == kWarpTma) {
     // ------------------------------------------------ any-K TMA producer --
     // Lane 0: per stage 8 + 8 A boxes (residue r: rows 8 i + r, i < 28 and
-    // i >= 28) and 16 W boxes (residue r: rows 16 i + r), each starting at the
-    // stage's K offset of its residue rounded down to 16 bytes.  All lanes:
-    // the rows past the last full group by 16-byte cp.async (a chunk that
-    // crosses the end of its buffer copies only the bytes inside it).
+    // i >= 28); lanes 0 .. R - 1: the R W boxes (residue r: rows R i + r),
+    // each box starting at the stage's K offset of its residue rounded down
+    // to 16 bytes.  All lanes: the rows past the last full group by 16-byte
+    // cp.async (a chunk that crosses the end of its buffer copies only the
+    // bytes inside it).
     const uint8_t* a_g = static_cast<const uint8_t*>(p.a_g);
     const int64_t K = p.K;
     const uint8_t* a_end = a_g + 2 * static_cast<int64_t>(p.M) * K;
     const uint8_t* w_end = p.w_g + static_cast<int64_t>(p.N) * K;
     const int a_full = 8 * p.a_groups;             // rows covered by the A maps
-    const int w_full = 16 * p.w_groups;            // rows covered by the W map
+    const int w_full = p.w_res * p.w_groups;      // rows covered by the W map
     // This CTA's rows of a tile (pair tiles: 256 A rows and 128 weight rows).
     auto cta_rows = [&](const Tile& tt, int& m0c, int& m1c, int& n0c, int& n1c) {
       m0c = tt.m0 + a_row0;
@@ -743,7 +745,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       tc::cp_async_16(dst, n ? src : any, n);
     };
     constexpr uint32_t kTx0 = LA::kABoxBytes, kTx1 = LA::kWBoxBytes;
-    constexpr uint32_t kWBoxStride = kPair ? kAnyPairWBox : kAnyWBox;   // one residue's W box
+    const uint32_t w_box = static_cast<uint32_t>(LA::kWRows / p.w_res) * kAnyRowW;   // one residue's W box
     // K % 8 == 0: A's rows are 16-byte strided and come as one plain tiled
     // box per stage (128-byte swizzle, the MMA's layout); only W needs the
     // residue boxes.
@@ -781,14 +783,14 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
                               g0 + kAnyInTile);
             }
           }
-          if (p.w_groups > 0) {
-            const int g0 = n0c / 16;
-#pragma unroll 1
-            for (int r = 0; r < 16; ++r) {
-              const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(15));
-              tc::tma_load_2d(st + LA::kWOff + r * kWBoxStride, &tmap_w, &full_raw[s], x0, g0);
-            }
-          }
+        }
+        __syncwarp();   // the stage's expected bytes are set before the W boxes go out
+        // W: one box per residue class (rows w_res i + r), issued by lanes
+        // 0 .. w_res - 1 in parallel.
+        if (p.w_groups > 0 && lane < p.w_res) {
+          const int r = lane;
+          const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(15));
+          tc::tma_load_2d(st + LA::kWOff + r * w_box, &tmap_w, &full_raw[s], x0, n0c / p.w_res);
         }
         if (a_part) {
           for (int c = lane; c < 7 * 9; c += 32) {
@@ -915,23 +917,29 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     // Thread t owns smem A row t (residue t / 32, group index t % 32) and one
     // weight row chosen so that the 8 threads of each quarter warp read
     // distinct 16-byte bank groups of the raw boxes and write distinct ones of
-    // the swizzled tile: residue u + 8 (g & 1), group index (u + g / 2) mod 16
-    // for t = 8 g + u.  Each raw window is shifted by its fixed misalignment,
-    // the K tail of the last stage is zeroed, and rows past the end are zero.
-    // Pair tiles (128 weight rows per CTA, group index mod 8): threads t and
-    // t + 128 share a weight row, each realigning and decoding half of it.
+    // the swizzled tile: with R = w_res residues, thread u takes residue
+    // u mod R and group index (u / R + rot) mod (rows / R), rot = (u mod R)
+    // mod 8 for R >= 8, else (u mod R) * 8 / R -- so that the rows' positions
+    // in the raw area differ mod 8 within every quarter warp.  Each raw window
+    // is shifted by its fixed misalignment, the K tail of the last stage is
+    // zeroed, and rows past the end are zero.  Pair tiles (128 weight rows
+    // per CTA): threads t and t + 128 share a weight row, each realigning and
+    // decoding half of it.
     constexpr int kWParts = kDeqWarps * 32 / LA::kWRows;   // threads per weight row
     constexpr int kWWords = 16 / kWParts;                  // code words per thread
-    constexpr uint32_t kWBoxStride = kPair ? kAnyPairWBox : kAnyWBox;
+    const int wres = p.w_res;
+    const int wlog = __ffs(wres) - 1;
+    const uint32_t w_box = static_cast<uint32_t>(LA::kWRows >> wlog) * kAnyRowW;
     const int t = threadIdx.x - kDeqWarp0 * 32;
     const int ar = t >> 5, ai = t & 31;               // A residue, group index
     const int u = t % LA::kWRows, wpart = t / LA::kWRows;
-    const int wr = (u & 7) + 8 * ((u >> 3) & 1);      // W residue
-    const int wi = ((u & 7) + (u >> 4)) & (LA::kWRows / 16 - 1);   // W group index
-    const int wrow = 16 * wi + wr;                    // W row in the CTA's part of the tile
+    const int wr = u & (wres - 1);                    // W residue
+    const int rot = wres >= 8 ? (wr & 7) : (wr << (3 - wlog));
+    const int wi = ((u >> wlog) + rot) & ((LA::kWRows >> wlog) - 1);   // W group index
+    const int wrow = (wi << wlog) + wr;               // W row in the CTA's part of the tile
     const int64_t K = p.K;
     const int a_full = 8 * p.a_groups;
-    const int w_full = 16 * p.w_groups;
+    const int w_full = wres * p.w_groups;
     const uint32_t off_a = static_cast<uint32_t>((2 * ar * K) & 15);
     const uint32_t off_w = static_cast<uint32_t>((wr * K) & 15);
     int s = 0;
@@ -947,7 +955,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
                                         : LA::kPartAOff + (m - a_full) * kAnyRowA;
       const int n = tl.n0 + w_row0 + wrow;
       const bool w_act = n < p.N;
-      const uint32_t w_src = (n < w_full ? LA::kWOff + wr * kWBoxStride + wi * kAnyRowW
+      const uint32_t w_src = (n < w_full ? LA::kWOff + wr * w_box + wi * kAnyRowW
                                          : LA::kPartWOff + (n - w_full) * kAnyRowW) +
                              32 * wpart;
       for (int kb = kb0; kb < nkb; ++kb) {
@@ -1538,7 +1546,9 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
     p.w_g = w;
     p.a_tma = K % 8 == 0 ? 1 : 0;
     p.a_groups = p.a_tma ? 0 : static_cast<int>(M / 8);
-    p.w_groups = static_cast<int>(N / 16);
+    // W rows w_res apart are 16-byte strided (w_res * K % 16 == 0).
+    p.w_res = (K & 1) ? 16 : (K & 3) ? 8 : (K & 7) ? 4 : 2;
+    p.w_groups = static_cast<int>(N / p.w_res);
     if (p.a_tma && !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, K * 2, BK, BM,
                               CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -1552,8 +1562,8 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
     // 128 weight rows: W boxes of 8 groups).
     const bool pair = M > BM;
     if (p.w_groups > 0 &&
-        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 16 * K, N / 16, 16 * K, kAnyRowW,
-                   pair ? kAnyPairWGroups : 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, p.w_res * K, N / p.w_res, p.w_res * K,
+                   kAnyRowW, (pair ? kPairWRows : BN) / p.w_res, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     if (pair) {
       p.bm = kPairBM;

@@ -51,7 +51,8 @@ def check(m, n, k, out_dtype=torch.float32, seed=0, rows=None, bias=None, act="n
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1), (3, 5, 7), (17, 33, 3), (200, 384, 520),
                                    (130, 257, 65), (257, 300, 129), (513, 700, 1001),
                                    (64, 4096, 4099), (300, 1000, 4100), (129, 520, 2),
-                                   (513, 700, 1000), (7, 40, 8), (260, 300, 24), (128, 256, 4104)])
+                                   (513, 700, 1000), (7, 40, 8), (260, 300, 24), (128, 256, 4104),
+                                   (5, 33, 4102), (100, 67, 12)])
 def test_anyk_shapes(m, n, k):
     lib()
     check(m, n, k, seed=m + n + k)
@@ -60,9 +61,12 @@ def test_anyk_shapes(m, n, k):
 # M > 256 runs on CTA pairs: each CTA realigns 256 rows of A (tile rows
 # 256 rank + [0, 256)) and decodes 128 weight rows.  Rows just past 256 and
 # 512, N below 16 (no weight box at all) or with the odd CTA's weight rows
-# partly or wholly past the end, K with and without the plain A box.
+# partly or wholly past the end, K with and without the plain A box, and
+# every W residue count R = 16 / gcd(K, 16) (2, 4, 8, 16) with N % R rows
+# past the last full group.
 @pytest.mark.parametrize("m,n,k", [(257, 129, 72), (511, 129, 100), (600, 200, 100), (777, 15, 33),
-                                   (1030, 130, 4104), (513, 260, 4100)])
+                                   (1030, 130, 4104), (513, 260, 4100), (700, 259, 4102),
+                                   (600, 131, 1004), (300, 1001, 4100)])
 def test_anyk_pair_edges(m, n, k):
     lib()
     check(m, n, k, seed=2 * m + n + k)
