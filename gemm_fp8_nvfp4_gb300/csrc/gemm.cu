@@ -709,10 +709,10 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
   } else if (kAnyK && warp == kWarpTma) {
     // ------------------------------------------------ any-K TMA producer --
-    // Lane 0: per stage 8 + 8 A boxes (residue r: rows 8 i + r, i < 28 and
-    // i >= 28); lanes 0 .. R - 1: the R W boxes (residue r: rows R i + r),
-    // each box starting at the stage's K offset of its residue rounded down
-    // to 16 bytes.  All lanes: the rows past the last full group by 16-byte
+    // Per stage, lanes 0 .. 15: 8 + 8 A boxes (residue r: rows 8 i + r, i < 28
+    // and i >= 28); lanes 16 .. 16 + R - 1: the R W boxes (residue r: rows
+    // R i + r), each box starting at the stage's K offset of its residue
+    // rounded down to 16 bytes.  All lanes: the rows past the last full group by 16-byte
     // cp.async (a chunk that crosses the end of its buffer copies only the
     // bytes inside it).
     const uint8_t* a_g = static_cast<const uint8_t*>(p.a_g);
@@ -773,22 +773,21 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           tc::mbar_arrive_expect_tx(&full_raw[s], tx);
           if (p.a_tma) {
             tc::tma_load_2d(st, &tmap_a, &full_raw[s], static_cast<int>(k0), m0c);
-          } else if (p.a_groups > 0) {
-            const int g0 = m0c / 8;
-#pragma unroll 1
-            for (int r = 0; r < 8; ++r) {
-              const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(7));
-              tc::tma_load_2d(st + any_raw_a_off(r, 0, LA::kSideOff), &tmap_a, &full_raw[s], x0, g0);
-              tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile, LA::kSideOff), &tmap_x, &full_raw[s], x0,
-                              g0 + kAnyInTile);
-            }
           }
         }
-        __syncwarp();   // the stage's expected bytes are set before the W boxes go out
-        // W: one box per residue class (rows w_res i + r), issued by lanes
-        // 0 .. w_res - 1 in parallel.
-        if (p.w_groups > 0 && lane < p.w_res) {
-          const int r = lane;
+        __syncwarp();   // the stage's expected bytes are set before the other boxes go out
+        // A (K % 8 != 0): the two boxes of residue r (rows 8 i + r, i < 28 and
+        // i >= 28) from lanes r and 8 + r; W: one box per residue class (rows
+        // w_res i + r) from lane 16 + r -- all issued in parallel.
+        if (!p.a_tma && p.a_groups > 0 && lane < 16) {
+          const int r = lane & 7;
+          const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(7));
+          if (lane < 8) tc::tma_load_2d(st + any_raw_a_off(r, 0, LA::kSideOff), &tmap_a, &full_raw[s], x0, m0c / 8);
+          else tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile, LA::kSideOff), &tmap_x, &full_raw[s], x0,
+                               m0c / 8 + kAnyInTile);
+        }
+        if (p.w_groups > 0 && lane >= 16 && lane < 16 + p.w_res) {
+          const int r = lane - 16;
           const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(15));
           tc::tma_load_2d(st + LA::kWOff + r * w_box, &tmap_w, &full_raw[s], x0, n0c / p.w_res);
         }
