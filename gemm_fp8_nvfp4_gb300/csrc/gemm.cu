@@ -359,6 +359,7 @@ struct Problem {
   int G, E, max_rows;          // grouped only
   int a_groups, w_groups;      // any-K path: full 8-row groups of A, w_res-row groups of W
   int w_res;                   // any-K path: W rows per 16-byte-strided group, 16 / gcd(K, 16)
+  int a_res;                   // any-K path, K % 8 != 0: A rows per group, 8 / gcd(K, 8)
   int tma_out;                 // 16-bit output stored through the output tensor map
   int a_tma;                   // any-K path with K % 8 == 0: A by the plain tiled map
   Epi ep;                      // output type and fused epilogue
@@ -455,11 +456,26 @@ __device__ __forceinline__ int num_tiles(const Problem& p) {
 
 // ------------------------------------------------------ any-K loading --
 
-// Where the raw window of residue r, group index i (tile row 8 i + r) of a
-// stage lands, relative to the stage (side_off: the layout's side area).
-__device__ __forceinline__ uint32_t any_raw_a_off(int r, int i, uint32_t side_off) {
-  return i < kAnyInTile ? static_cast<uint32_t>(r * 4096 + i * kAnyRowA)
-                        : side_off + r * kAnySideSlot + (i - kAnyInTile) * kAnyRowA;
+// A CTA's 256 rows of A in R residue classes (rows R i + r, R = 2, 4 or 8):
+// rr = 256 / R rows per class, whose realigned rows occupy smem rows
+// rr r .. rr r + rr - 1 (128 rr bytes).  The first ip = floor(128 rr / 144)
+// raw windows of class r land in place inside those bytes, the other
+// rr - ip in the class's side slot (rounded up to 128 bytes).
+__host__ __device__ constexpr int any_a_in_place(int R) { return (256 / R) * 128 / static_cast<int>(kAnyRowA); }
+__host__ __device__ constexpr uint32_t any_a_side_slot(int R) {
+  return ((static_cast<uint32_t>(256 / R - any_a_in_place(R)) * kAnyRowA + 127u) / 128u) * 128u;
+}
+static_assert(any_a_in_place(8) == kAnyInTile && any_a_side_slot(8) == kAnySideSlot,
+              "eight classes: 28 rows in place, 4 in a 640-byte slot");
+static_assert(2 * any_a_side_slot(2) <= 8 * kAnySideSlot && 4 * any_a_side_slot(4) <= 8 * kAnySideSlot,
+              "the side slots of every class count fit the side area");
+
+// Where the raw window of class r (of R), group index i (tile row R i + r) of
+// a stage lands, relative to the stage (side_off: the layout's side area).
+__device__ __forceinline__ uint32_t any_raw_a_off(int R, int r, int i, uint32_t side_off) {
+  const int ip = any_a_in_place(R);
+  return i < ip ? static_cast<uint32_t>(r * (256 / R) * 128 + i * kAnyRowA)
+                : side_off + r * any_a_side_slot(R) + (i - ip) * kAnyRowA;
 }
 
 // The bytes [off, off + 4 N) of in[] (off = 0..15, a per-row constant), as
@@ -709,17 +725,17 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     }
   } else if (kAnyK && warp == kWarpTma) {
     // ------------------------------------------------ any-K TMA producer --
-    // Per stage, lanes 0 .. 15: 8 + 8 A boxes (residue r: rows 8 i + r, i < 28
-    // and i >= 28); lanes 16 .. 16 + R - 1: the R W boxes (residue r: rows
-    // R i + r), each box starting at the stage's K offset of its residue
-    // rounded down to 16 bytes.  All lanes: the rows past the last full group by 16-byte
+    // Per stage, lanes 0 .. 2 R_A - 1: R_A + R_A A boxes (class r: rows
+    // R_A i + r, i < ip and i >= ip); lanes 16 .. 16 + R_W - 1: the R_W W boxes
+    // (class r: rows R_W i + r), each box starting at the stage's K offset of
+    // its class rounded down to 16 bytes.  All lanes: the rows past the last full group by 16-byte
     // cp.async (a chunk that crosses the end of its buffer copies only the
     // bytes inside it).
     const uint8_t* a_g = static_cast<const uint8_t*>(p.a_g);
     const int64_t K = p.K;
     const uint8_t* a_end = a_g + 2 * static_cast<int64_t>(p.M) * K;
     const uint8_t* w_end = p.w_g + static_cast<int64_t>(p.N) * K;
-    const int a_full = 8 * p.a_groups;             // rows covered by the A maps
+    const int a_full = p.a_res * p.a_groups;      // rows covered by the A maps
     const int w_full = p.w_res * p.w_groups;      // rows covered by the W map
     // This CTA's rows of a tile (pair tiles: 256 A rows and 128 weight rows).
     auto cta_rows = [&](const Tile& tt, int& m0c, int& m1c, int& n0c, int& n1c) {
@@ -776,15 +792,16 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
           }
         }
         __syncwarp();   // the stage's expected bytes are set before the other boxes go out
-        // A (K % 8 != 0): the two boxes of residue r (rows 8 i + r, i < 28 and
-        // i >= 28) from lanes r and 8 + r; W: one box per residue class (rows
+        // A (K % 8 != 0): the two boxes of class r (rows R i + r, i < ip and
+        // i >= ip) from lanes r and R + r; W: one box per class (rows
         // w_res i + r) from lane 16 + r -- all issued in parallel.
-        if (!p.a_tma && p.a_groups > 0 && lane < 16) {
-          const int r = lane & 7;
+        if (!p.a_tma && p.a_groups > 0 && lane < 2 * p.a_res) {
+          const int R = p.a_res;
+          const int r = lane & (R - 1);
           const int x0 = static_cast<int>((r * K + k0) & ~static_cast<int64_t>(7));
-          if (lane < 8) tc::tma_load_2d(st + any_raw_a_off(r, 0, LA::kSideOff), &tmap_a, &full_raw[s], x0, m0c / 8);
-          else tc::tma_load_2d(st + any_raw_a_off(r, kAnyInTile, LA::kSideOff), &tmap_x, &full_raw[s], x0,
-                               m0c / 8 + kAnyInTile);
+          if (lane < R) tc::tma_load_2d(st + any_raw_a_off(R, r, 0, LA::kSideOff), &tmap_a, &full_raw[s], x0, m0c / R);
+          else tc::tma_load_2d(st + any_raw_a_off(R, r, any_a_in_place(R), LA::kSideOff), &tmap_x, &full_raw[s],
+                               x0, m0c / R + any_a_in_place(R));
         }
         if (p.w_groups > 0 && lane >= 16 && lane < 16 + p.w_res) {
           const int r = lane - 16;
@@ -930,14 +947,16 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
     const int wlog = __ffs(wres) - 1;
     const uint32_t w_box = static_cast<uint32_t>(LA::kWRows >> wlog) * kAnyRowW;
     const int t = threadIdx.x - kDeqWarp0 * 32;
-    const int ar = t >> 5, ai = t & 31;               // A residue, group index
+    const int ares = p.a_res;                         // A classes (K % 8 != 0)
+    const int arlog = 8 - (__ffs(ares) - 1);          // log2 of the rows per class, 256 / ares
+    const int ar = t >> arlog, ai = t & ((1 << arlog) - 1);   // A class, group index
     const int u = t % LA::kWRows, wpart = t / LA::kWRows;
     const int wr = u & (wres - 1);                    // W residue
     const int rot = wres >= 8 ? (wr & 7) : (wr << (3 - wlog));
     const int wi = ((u >> wlog) + rot) & ((LA::kWRows >> wlog) - 1);   // W group index
     const int wrow = (wi << wlog) + wr;               // W row in the CTA's part of the tile
     const int64_t K = p.K;
-    const int a_full = 8 * p.a_groups;
+    const int a_full = ares * p.a_groups;
     const int w_full = wres * p.w_groups;
     const uint32_t off_a = static_cast<uint32_t>((2 * ar * K) & 15);
     const uint32_t off_w = static_cast<uint32_t>((wr * K) & 15);
@@ -948,9 +967,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
       const Tile tl = get_tile<kGrouped>(p, tt);
       if (!tl.valid || tl.expert < 0) continue;
       const int m0c = tl.m0 + a_row0;                 // this CTA's rows of the tile
-      const int m = m0c + 8 * ai + ar;
+      const int m = m0c + ares * ai + ar;
       const bool a_act = m < min(m0c + BM, tl.m_end);
-      const uint32_t a_src = m < a_full ? any_raw_a_off(ar, ai, LA::kSideOff)
+      const uint32_t a_src = m < a_full ? any_raw_a_off(ares, ar, ai, LA::kSideOff)
                                         : LA::kPartAOff + (m - a_full) * kAnyRowA;
       const int n = tl.n0 + w_row0 + wrow;
       const bool w_act = n < p.N;
@@ -958,7 +977,11 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
                                          : LA::kPartWOff + (n - w_full) * kAnyRowW) +
                              32 * wpart;
       for (int kb = kb0; kb < nkb; ++kb) {
-        if (!tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant)) {
+        const bool got = tc::mbar_wait(&full_raw[s], ph, abort_flag, p.status, kStatusTimeoutDequant);
+        // With fewer than eight A classes the dequant warps meet at a named
+        // barrier each stage, so a failed wait is voted there and every
+        // participant leaves together; otherwise each thread leaves at once.
+        if (!got && (p.a_tma || ares == 8)) {
           ok = false;
           break;
         }
@@ -966,7 +989,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         const uint32_t st = smem_base + s * LA::kStage;
         if (!p.a_tma) {
           uint32_t out[32];
-          if (a_act) {
+          if (got && a_act) {
             uint32_t in[36];
 #pragma unroll
             for (int c = 0; c < 9; ++c) {
@@ -979,7 +1002,15 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
 #pragma unroll
             for (int i = 0; i < 32; ++i) out[i] = 0u;
           }
-          __syncwarp();                             // every raw row of the warp is read
+          // Every raw row is read before a realigned row overwrites it: the
+          // warp's own rows with eight classes (one warp per class), all
+          // dequant warps' with fewer (a class spans several warps).
+          if (ares == 8) {
+            __syncwarp();
+          } else if (tc::bar_red_or<1, kDeqWarps * 32>(!got)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             tc::sts128(st + sw128_off(t, c),
@@ -1230,7 +1261,9 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
         // Lane 32 g + lane of TMEM half h holds tile row h * 128 + 32 g + lane
         // (pair tiles: h * 256 + 128 rank + 32 g + lane), or (any K, residue
         // order) tile row 8 lane + 4 h + g.
-        const int m = residue_rows ? tl.m0 + a_row0 + 8 * lane + 4 * h + g
+        const int srow = 128 * h + 32 * g + lane;   // residue order: class srow / rr, group srow % rr
+        const int rlog = 8 - (__ffs(p.a_res) - 1);
+        const int m = residue_rows ? tl.m0 + a_row0 + p.a_res * (srow & ((1 << rlog) - 1)) + (srow >> rlog)
                                    : tl.m0 + h * kHalfRows + a_row0 + g * 32 + lane;
         const bool row_ok = m < tl.m_end;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) + h * BN;
@@ -1544,7 +1577,9 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
     p.a_g = a;
     p.w_g = w;
     p.a_tma = K % 8 == 0 ? 1 : 0;
-    p.a_groups = p.a_tma ? 0 : static_cast<int>(M / 8);
+    // A rows a_res apart are 16-byte strided (2 a_res K % 16 == 0).
+    p.a_res = (K & 1) ? 8 : (K & 3) ? 4 : 2;
+    p.a_groups = p.a_tma ? 0 : static_cast<int>(M / p.a_res);
     // W rows w_res apart are 16-byte strided (w_res * K % 16 == 0).
     p.w_res = (K & 1) ? 16 : (K & 3) ? 8 : (K & 7) ? 4 : 2;
     p.w_groups = static_cast<int>(N / p.w_res);
@@ -1552,10 +1587,10 @@ cudaError_t launch_fp8_gemm(const Ctx& c, void* out, const Epi& ep, const void* 
                               CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     if (p.a_groups > 0 &&
-        (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72, kAnyInTile,
-                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-         !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, 8 * K, M / 8, 16 * K, 72,
-                    32 - kAnyInTile, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, p.a_res * K, M / p.a_res, 2 * p.a_res * K,
+                    72, any_a_in_place(p.a_res), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, p.a_res * K, M / p.a_res, 2 * p.a_res * K,
+                    72, 256 / p.a_res - any_a_in_place(p.a_res), CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
     // M > 256: pair tiles (each CTA realigns its 256 rows of A and decodes
     // 128 weight rows: W boxes of 8 groups).

@@ -63,10 +63,12 @@ def test_anyk_shapes(m, n, k):
 # 512, N below 16 (no weight box at all) or with the odd CTA's weight rows
 # partly or wholly past the end, K with and without the plain A box, and
 # every W residue count R = 16 / gcd(K, 16) (2, 4, 8, 16) with N % R rows
-# past the last full group.
+# past the last full group, and every A class count 8 / gcd(K, 8) (2, 4, 8)
+# with M % R_A rows past the last full group.
 @pytest.mark.parametrize("m,n,k", [(257, 129, 72), (511, 129, 100), (600, 200, 100), (777, 15, 33),
                                    (1030, 130, 4104), (513, 260, 4100), (700, 259, 4102),
-                                   (600, 131, 1004), (300, 1001, 4100)])
+                                   (600, 131, 1004), (300, 1001, 4100), (515, 64, 70),
+                                   (701, 40, 4102)])
 def test_anyk_pair_edges(m, n, k):
     lib()
     check(m, n, k, seed=2 * m + n + k)
