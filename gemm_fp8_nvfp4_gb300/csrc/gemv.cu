@@ -54,11 +54,14 @@ constexpr int kThreads = 128;   // threads per CTA
 // CTA's first weight bytes start moving from HBM into L2 during its tail and
 // the loads after the wait find them there.  FP8: the CTA's rows in one
 // prefetch when they total at most kPrefetchCtaBytes, else the first
-// kPrefetchRowHead bytes of each row (prefetching whole long rows competes
-// with the loads: 4096 x 14336 took 13.7 us instead of 10.1 us).  NVFP4: the
-// CTA's codes and block scales, one prefetch each (at most kPrefetchMax).
+// kPrefetchRowHead bytes of each row: more competes with the loads (whole
+// 14 KB rows: 4096 x 14336 took 13.7 us instead of 10.1 us; for the three
+// decode shapes back to back with 8-row CTAs at K = 4096, a row head of 2 KB
+// or 3 KB ran 3-10 % slower than 1.25 KB, and none at all 9 % slower).
+// NVFP4: the CTA's codes and block scales, one prefetch each (at most
+// kPrefetchMax).
 constexpr int64_t kPrefetchCtaBytes = 16384;
-constexpr int64_t kPrefetchRowHead = 2048;
+constexpr int64_t kPrefetchRowHead = 1280;
 constexpr int64_t kPrefetchMax = 65536;
 
 // L2 prefetch of the 16-byte-aligned part of [p, p + min(bytes, cap)).
