@@ -119,9 +119,14 @@ k_fewrow(void* __restrict__ out, Epi ep, const uint16_t* __restrict__ a,
   const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * N / gridDim.x;
   const int64_t rbytes = F == kFewFp8 ? K : K / 2;     // weight bytes per row
   pdl_launch_dependents();
+  // L2 prefetch of each row before the wait (a prefetch returns no data).
+  // FP8: the whole row (up to 64 KB).  NVFP4: the first 1 KB of the codes and
+  // the row's block scales -- at M = 16 and N = K = 4096 7.54 us against
+  // 7.70 us with the whole codes and no scales (M = 8: 5.78 / 5.93 us).
+  constexpr int64_t kHead = F == kFewFp8 ? 65536 : 1024;
   for (int64_t r = r_begin + threadIdx.x; r < r_end; r += kThreads) {
-    // a prefetch returns no data: it may run before the wait
-    tc::bulk_prefetch_l2(w + r * rbytes, static_cast<uint32_t>(rbytes < 65536 ? rbytes : 65536));
+    tc::bulk_prefetch_l2_span(w + r * rbytes, rbytes < kHead ? rbytes : kHead);
+    if constexpr (F == kFewNvfp4) tc::bulk_prefetch_l2_span(bs + r * (K / 16), K / 16 < 65536 ? K / 16 : 65536);
   }
   pdl_wait();
 

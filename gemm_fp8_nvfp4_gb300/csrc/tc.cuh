@@ -184,6 +184,14 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* addr, uint32_t byte
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
 
+// L2 prefetch of the 16-byte-aligned interior of [p, p + bytes) (nothing if
+// that is empty): any pointer and length.
+__device__ __forceinline__ void bulk_prefetch_l2_span(const void* p, uint64_t bytes) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
+  if (e > a) bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
