@@ -585,13 +585,16 @@ def w8a8_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
     x = synth.bf16_activations(m, k, seed=1)
     copies = max(2, int(math.ceil(2 * L2_BYTES / (n * k + 2 * m * k))))
     ins = [(x.to(dev), qb.to(dev)) for _ in range(copies)]
+    # The quantizer reads only x: enough copies of it alone to exceed L2.
+    xcopies = max(2, int(math.ceil(2 * L2_BYTES / (2 * m * k))))
+    xs = [x.to(dev) for _ in range(xcopies)]
     d_sb = sb.to(dev)
     qa = torch.empty((m, k), dtype=torch.int8, device=dev)
     sa = torch.empty((m,), dtype=torch.float32, device=dev)
     out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
 
     def quant_step(i):
-        gq.int8_quantize_rows(ins[i % copies][0], q=qa, scale=sa, stream=stream)
+        gq.int8_quantize_rows(xs[i % xcopies], q=qa, scale=sa, stream=stream)
 
     def gemm_step(i):
         gq.int8_matmul(qa, ins[i % copies][1], sa, d_sb, out=out, stream=stream)
@@ -612,8 +615,8 @@ def w8a8_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
         "gemm_us": round(tg * 1e6, 2), "gemm_TFLOP/s": round(tfl, 1),
         "gemm_frac_bf16_tensor": round(tfl / peaks["bf16_tflops"], 4),
         "step_us": round(tb * 1e6, 2),
-        "l2": f"{copies} rotating input copies"}
-    del ins
+        "l2": f"{xcopies} rotating activation copies (quantizer), {copies} rotating input copies (GEMM)"}
+    del ins, xs
 
 
 def grouped_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
