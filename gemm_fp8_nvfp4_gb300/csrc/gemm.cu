@@ -635,7 +635,7 @@ k_wq_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CU
   const int kb1 = split ? min(p.num_k_blocks, kb0 + p.kb_per_split) : p.num_k_blocks;
   const int nkb = kb1;
 
-  if (warp == kWarpTma && !kAnyK && p.stall_producer) {
+  if (warp == kWarpTma && p.stall_producer) {
     // Failure-path test: no copy is issued, so every stage stays empty and
     // the other roles' bounded waits run out (nothing asynchronous to drain).
   } else if (warp == kWarpTma && !kAnyK) {
@@ -1453,7 +1453,7 @@ cudaError_t launch(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tw, c
   auto kern = k_wq_gemm<F, kGrouped, kAnyK, kPair>;
   const uint32_t smem = SmemFor<F, kAnyK, kPair>::kAlloc;
   Problem pl = p;
-  pl.stall_producer = (!kAnyK && c.test_stall_producer) ? 1 : 0;
+  pl.stall_producer = c.test_stall_producer ? 1 : 0;
   // The shared-memory opt-in is set once per device (it is not a stream
   // operation, so it is kept out of any CUDA-graph capture after the first call).
   static std::atomic<uint64_t> configured{0};

@@ -129,8 +129,9 @@ typedef struct gq_epilogue {
 #define GQ_LAUNCH_OVERLAP_WEIGHT_READS 1u
 /*
  * GQ_LAUNCH_TEST_STALL_PRODUCER (tests only; never set it for real work):
- * the tensor-core GEMM for M > 128 (FP8, NVFP4, W8A8 and grouped; not the
- * few-row, any-K or GEMV kernels) launches with its copy producer idle, so
+ * the persistent tensor-core GEMM (FP8 and NVFP4 with M > 128, FP8 with any
+ * K, W8A8, grouped; not the few-row, M <= 128 split-K or GEMV kernels)
+ * launches with its copy producer idle, so
  * no shared-memory stage ever fills, nothing asynchronous is issued, and every
  * bounded wait of the kernel runs out: the call returns, the output is left
  * unwritten, and gq_device_status reports the timed-out waits.  Use it with a

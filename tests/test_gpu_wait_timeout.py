@@ -84,8 +84,8 @@ def test_stalled_producer_times_out_and_recovers(fmt):
 
 
 def test_stalled_w8a8_split_k_times_out_and_recovers():
-    """The W8A8 GEMM with K split over a cluster of 2 (K = 16384): every CTA of
-    the cluster times out, none adds a partial, both leave the cluster
+    """The W8A8 GEMM with K split over a cluster (M = 5, K = 16384): every CTA
+    of the cluster times out, none adds a partial, all leave the cluster
     barriers, and the next call is bit-exact."""
     lib()
     m, n, k = 5, 256, 16384
@@ -102,4 +102,31 @@ def test_stalled_w8a8_split_k_times_out_and_recovers():
     torch.cuda.synchronize()
     want = oracle.int8_matmul(qa.numpy(), qb.numpy(), sa.numpy(), sb.numpy())
     assert np.array_equal(c.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert gq.device_status() == 0
+
+
+@pytest.mark.parametrize("k", [100, 33, 104])
+def test_stalled_anyk_times_out_and_recovers(k):
+    """The FP8 GEMM with K % 16 != 0 on CTA pairs (M > 256): K = 100 realigns A
+    in two residue classes whose rows span several dequant warps (their
+    named barrier also votes on a failed wait), K = 33 in eight classes of
+    one warp each, K = 104 takes A by the tiled box.  Every role's wait runs
+    out, all leave together, and the next call is correct."""
+    lib()
+    m, n = 300, 256
+    a = synth.bf16_activations(m, k, seed=5)
+    codes, s = synth.fp8_weight(n, k, seed=6)
+    w_hat = oracle.decode_fp8(codes.numpy())
+    out = torch.full((m, n), 7.25, dtype=torch.float32, device=DEV)
+    run = lambda o: gq.fp8_matmul(a.to(DEV), codes.to(DEV), s, out=o)
+    dt, st = stalled(lambda: run(out))
+    assert dt < 5.0, f"the stalled call took {dt:.2f} s"
+    check_recovered(st)
+    assert torch.all(out == 7.25), "a stalled GEMM wrote its output"
+    c = torch.empty((m, n), dtype=torch.float32, device=DEV)
+    run(c)
+    torch.cuda.synchronize()
+    ab = bits(a)
+    ref = oracle.linear(ab, w_hat, s)
+    assert_within(to_f64(c), ref, oracle.tolerance(ab, w_hat, s), f"any-K {k} after time-out")
     assert gq.device_status() == 0
