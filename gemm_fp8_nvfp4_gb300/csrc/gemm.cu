@@ -219,8 +219,10 @@ struct SmemAnyK {
 constexpr int kPairBM = 512;
 constexpr int kPairWRows = BN / 2;
 template <Fmt F> struct SmemPair {
-  static constexpr int kRawSt = 4;
-  static constexpr int kDeqSt = 2;
+  // 3 raw + 3 decoded stages: M = 2048 FP8 143.2 us against 145.4 us with
+  // 4 + 2 (3 + 4: 143.9, 3 + 2: 145.9, 2 + 4: 189.6).
+  static constexpr int kRawSt = 3;
+  static constexpr int kDeqSt = 3;
   static constexpr int kWRows = kPairWRows;
   static constexpr uint32_t kWBytes = RawLayout<F>::kWBytes / 2;
   static constexpr uint32_t kScaleBytes = RawLayout<F>::kScaleBytes / 2;
