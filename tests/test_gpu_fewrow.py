@@ -51,7 +51,8 @@ def test_every_row_count(fmt, m):
 
 @pytest.mark.parametrize("fmt,n,k", [("fp8", 1, 64), ("fp8", 17, 128), ("fp8", 1000, 4096),
                                      ("fp8", 333, 8192), ("nvfp4", 1, 128), ("nvfp4", 15, 256),
-                                     ("nvfp4", 1000, 4096), ("nvfp4", 300, 14336)])
+                                     ("nvfp4", 1000, 4096), ("nvfp4", 300, 14336),
+                                     ("nvfp4", 37, 384), ("nvfp4", 9, 640)])
 def test_shapes(fmt, n, k):
     lib()
     for m in (3, 9, 16):
