@@ -237,6 +237,13 @@ def n_copies(bytes_per_set: int) -> int:
     return max(2, int(math.ceil(ROTATION_TARGET / max(1, bytes_per_set))))
 
 
+def copies_past_l2(bytes_per_copy: int) -> int:
+    """Rotating copies of a sub-benchmark's inputs so that one rotation reads
+    at least twice the L2 capacity (consecutive launches find nothing of
+    their inputs in L2)."""
+    return max(2, int(math.ceil(2 * L2_BYTES / max(1, bytes_per_copy))))
+
+
 def make_fp8_gemv_sets(dev):
     import synth
     base = []
@@ -537,7 +544,7 @@ def gemm_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
     m, n, k = 2048, 14336, 4096
     codes, s = synth.fp8_weight(n, k, seed=0)
     a = synth.bf16_activations(m, k, seed=1)
-    copies = max(2, int(math.ceil(2 * L2_BYTES / (n * k + 2 * m * k))))
+    copies = copies_past_l2(n * k + 2 * m * k)
     ins = [(a.to(dev), codes.to(dev)) for _ in range(copies)]
     out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
 
@@ -583,10 +590,10 @@ def w8a8_sub(gq, dev, stream, peaks, world, gsteps, warm, subs):
     m, n, k = 2048, 14336, 4096
     qb, sb = synth.int8_weight(n, k, seed=0)
     x = synth.bf16_activations(m, k, seed=1)
-    copies = max(2, int(math.ceil(2 * L2_BYTES / (n * k + 2 * m * k))))
+    copies = copies_past_l2(n * k + 2 * m * k)
     ins = [(x.to(dev), qb.to(dev)) for _ in range(copies)]
     # The quantizer reads only x: enough copies of it alone to exceed L2.
-    xcopies = max(2, int(math.ceil(2 * L2_BYTES / (2 * m * k))))
+    xcopies = copies_past_l2(2 * m * k)
     xs = [x.to(dev) for _ in range(xcopies)]
     d_sb = sb.to(dev)
     qa = torch.empty((m, k), dtype=torch.int8, device=dev)

@@ -60,3 +60,14 @@ def test_committed_traffic_file_is_well_formed():
     for ent in d.values():
         assert os.path.exists(os.path.join(bench.ROOT, ent["source"]))
         assert len(ent["source_sha256_16"]) == 16 and ent["bytes_per_launch"] > 0
+
+
+@pytest.mark.parametrize("bytes_per_copy", [
+    14336 * 4096 + 2 * 2048 * 4096,    # FP8 / W8A8 GEMM M = 2048: weights + activations
+    14336 * 4100 + 2 * 2048 * 4100,    # any-K GEMM
+    2 * 2048 * 4096,                   # W8A8 quantizer: the activations alone
+    1, 3 * bench.L2_BYTES])
+def test_sub_benchmark_rotation_exceeds_l2(bytes_per_copy):
+    copies = bench.copies_past_l2(bytes_per_copy)
+    assert copies >= 2
+    assert copies * bytes_per_copy >= 2 * bench.L2_BYTES
